@@ -1,0 +1,405 @@
+"""Benchmark: fused decompress + matmul on the Llama-3.1-8B-shaped gate_proj W[14336,4096].
+
+One step = one uw_matmul of the autotuned plan (AUTO) at B=1 on a Huffman-coded
+matrix loaded with its resident palette form, i.e. one pass of the whole hot
+path: strategy lookup, (preprocess if the plan has one), on-chip BF16
+reconstruction and the contraction.  Inputs are larger than L2: the step rotates
+over several device copies of the compressed matrix (each copy its own uw_matrix),
+so every step streams its weights from HBM.  Steps are replayed through CUDA
+graphs captured from the same C-ABI calls.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
+plain C decoder + fp64 matmul) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 2 ** 20
+WORKLOAD = "gate_8b"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--no-breakdown", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-autotune", action="store_true")
+    p.add_argument("--json-out", default=None)
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(info, strategy, B, out_bytes=4):
+    """Bytes a pass must move at minimum: the compressed stream the strategy reads, X and Y."""
+    N, K = info["N"], info["K"]
+    n = N * K
+    words = (info["n_blocks"] + 31) // 32
+    common = n + 64 * info["n_verbatim"] + 8 * words  # sm bytes, verbatim exponents, bitmap + prefix
+    if strategy == 4:   # direct palette: resident 4-bit codes
+        w = common + n // 2
+    else:               # Huffman-fed pipelines read the bit stream and its chunk offsets
+        w = common + (info["total_bits"] + 7) // 8 + 4 * (info["n_chunks"] + 1)
+    return w + 2 * B * K + out_bytes * B * N
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.gpu = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-i", str(self.gpu), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except Exception:
+                pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id(dev):
+    """nvidia-smi selector of the CUDA device in use (UUID; CUDA_VISIBLE_DEVICES may remap indices)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (reference arm / baseline)
+def oracle_step_seconds(blob, w_shape, x_np, steps):
+    """The oracle as it stands: decode the blob (plain C) and the fp64 matmul, `steps` times."""
+    import oracle
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        w = oracle.decode(blob)
+        oracle.matmul(w, x_np)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import lossless_bf16_weight_exponent_gb300 as uw
+    import oracle
+    import synth
+    oracle.build()
+    mat = synth.gate_8b()
+    w = mat.weights()
+    blob = oracle.encode(w, oracle.HUFFMAN)
+    x = mat.activations(args.batch)
+    steps = max(1, min(args.steps, 3))
+    warm = min(args.warmup, 1)
+    if warm:
+        oracle_step_seconds(blob, w.shape, x, warm)
+    times = oracle_step_seconds(blob, w.shape, x, steps)
+    sec = sum(times) / len(times)
+    eff = (2 * mat.N * mat.K + 2 * args.batch * mat.K + 4 * args.batch * mat.N) / sec / 1e9
+    line = {
+        "impl": "reference", "metric": "effective BF16 weight GB/s, fused decompress+matmul (B=%d)" % args.batch,
+        "value": eff, "unit": "GB/s", "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": f"{WORKLOAD} W[14336,4096] bf16 N(0,0.02)+1e-4x100, Huffman blob",
+                                         "batch": args.batch},
+        "cpu_baseline": {"value": eff, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} full steps: decode of the Huffman blob + fp64 GEMV (B={args.batch})"},
+        "e2e": {"value": eff, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    import synth
+
+    rank, world, local = dist_setup()
+    dev = torch.cuda.current_device()
+    B = args.batch
+    mat = synth.gate_8b()
+    w = mat.weights()
+    blob = uw.encode(w, uw.CODEC_HUFFMAN)
+    base = uw.Matrix(blob, want_palette_form=True)
+    info = base.info
+    resident = info["device_bytes"]
+    copies = max(2, int(np.ceil(3 * L2_BYTES / max(1, resident))))
+    mats = [base] + [uw.Matrix(blob, want_palette_form=True) for _ in range(copies - 1)]
+
+    # autotune on one copy (batches of the workload), share the table with the others
+    tune_batches = [1, 4, 16] if B in (1, 4, 16) else [B]
+    if not args.no_autotune:
+        need = base.autotune_workspace_size(tune_batches)
+        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        base.autotune(tune_batches, tws, need)
+        del tws
+        table = base.tune_save()
+        for m in mats[1:]:
+            m.tune_load(table)
+    plan = base.plan_for(B)
+    ws_bytes = max(m.workspace_size(B) for m in mats)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+    y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(i, s):
+        mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+
+    # CUDA graphs of G steps each, replayed to reach exactly K steps
+    K, W = args.steps, args.warmup
+    G = min(64, K)
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(n):  # warm the plan outside capture once
+                    step(i, stream)
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        step(i, stream)
+            graphs[n] = g
+        return graphs[n]
+
+    def run_steps(n):
+        full, rem = divmod(n, G)
+        gf = graph_for(G) if full else None
+        gr = graph_for(rem) if rem else None
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                gf.replay()
+            if gr is not None:
+                gr.replay()
+
+    run_steps(max(W, 3))
+    stream.synchronize()
+    clocks = Clocks(gpu_id(dev))
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run_steps(K)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
+    ms_step = ms_total / K
+
+    hbm_peak, tf_peak, peak_kind = peaks()
+    alg = algorithmic_bytes(info, plan.strategy, B)
+    eff_bytes = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+    value = eff_bytes * world * K / (ms_total * 1e-3) / 1e9
+
+    # kernels launched per step by this plan
+    launches_per_step = 1 + (plan.strategy != uw.STRAT_DIRECT_PALETTE)
+    if plan.split_k > 1:
+        launches_per_step += 0  # split accumulation uses a memset node and atomics, no extra kernel for fp32 out
+
+    # e2e through the public API with host buffers: H2D of X and D2H of Y inside the timed region
+    xh = torch.from_numpy(mat.activations(B).view(np.int16)).pin_memory()
+    yh = torch.empty((B, mat.N), dtype=torch.float32).pin_memory()
+    hneed = max(m.host_workspace_size(B) for m in mats)
+    hws = torch.empty(hneed, dtype=torch.uint8, device="cuda")
+    e2e_steps = min(max(K, 10), 2000)
+    for i in range(20):
+        mats[i % copies].matmul_host(xh, B, yh, uw.OUT_F32, hws, hneed, stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        mats[i % copies].matmul_host(xh, B, yh, uw.OUT_F32, hws, hneed, stream)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = eff_bytes * world * e2e_steps / e2e_s / 1e9
+
+    breakdown = {}
+    if not args.no_breakdown and rank == 0:
+        breakdown = strategy_breakdown(mats, mat, info, copies, hbm_peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(blob, w, mat, B)
+
+    if rank == 0:
+        achieved = alg / (ms_step * 1e-3) / 1e9
+        line = {
+            "metric": "effective BF16 weight GB/s, fused decompress+matmul (B=%d)" % B,
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(W, 3),
+            "ms_per_step": ms_step, "us_per_matmul": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: W[14336,4096] bf16 N(0,0.02) with 1e-4 of entries x100, "
+                                   f"Huffman blob + resident palette form; X[{B},4096] N(0,1)",
+                       "batch": B, "plan": plan.as_tuple(), "copies_rotated": copies,
+                       "l2": f"inputs larger than L2: {copies} copies x {resident / 1e6:.1f} MB resident",
+                       "compression": {"huffman_bits_per_weight": 8 * info["blob_bytes"] / (mat.N * mat.K),
+                                       "verbatim_block_fraction": info["n_verbatim"] / info["n_blocks"]}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": alg, "kernel": "gemv_kernel (fused reconstruct)"},
+            "effective_frac_of_peak": value / world / hbm_peak,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * B * mat.K,
+                    "d2h_bytes_per_step": 4 * B * mat.N, "us_per_call": e2e_s / e2e_steps * 1e6},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "breakdown": breakdown,
+        }
+        s = json.dumps(line)
+        print(s, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(s + "\n")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def strategy_breakdown(mats, mat, info, copies, hbm_peak):
+    """Per (B, strategy) timing of single calls rotating the copies (eager launches, L2 not warm)."""
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    out = {}
+    names = {1: "full_decode", 2: "exp_only", 3: "palette_transcode", 4: "direct_palette"}
+    for B in (1, 4, 16):
+        x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+        y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+        eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+        row = {}
+        for s, nm in names.items():
+            need = mats[0].workspace_size(B, s)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+            for i in range(6):
+                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
+            st = torch.cuda.current_stream()
+            reps = 40
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+            for i in range(reps):
+                ev[2 * i].record(st)
+                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
+                ev[2 * i + 1].record(st)
+            torch.cuda.synchronize()
+            us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(reps))
+            alg = algorithmic_bytes(info, s, B)
+            row[nm] = {"us": round(us, 2), "eff_GBps": round(eff / us / 1e3, 1),
+                       "compressed_GBps": round(alg / us / 1e3, 1), "compressed_frac": round(alg / us / 1e3 / hbm_peak, 3)}
+        auto = mats[0].plan_for(B)
+        row["auto_plan"] = auto.as_tuple()
+        out[f"B={B}"] = row
+    return out
+
+
+def cpu_baseline(blob, w, mat, B):
+    x = mat.activations(B)
+    times = oracle_step_seconds(blob, w.shape, x, 2)
+    sec = sum(times) / len(times)
+    eff = (2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N) / sec / 1e9
+    return {"value": eff, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"2 full steps: plain-C decode of the Huffman blob + fp64 GEMV at B={B}"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

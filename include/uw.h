@@ -1,0 +1,246 @@
+/*
+ * uw.h - C ABI of the lossless BF16 exponent codec with fused decode+matmul.
+ *
+ * Method: Cloudflare blog post "Unweight" (lossless compression of BF16 model
+ * weights, decompressed on-chip inside the matrix multiply).  Each BF16 weight
+ * is split into a raw sign+mantissa byte and an exponent byte; the exponent
+ * byte is coded against a per-matrix palette of the 16 most frequent exponents
+ * (4-bit codes) or with a length-limited canonical Huffman code; any run of 64
+ * weights holding an exponent outside the palette is stored verbatim.
+ *
+ * Conventions for every entry point:
+ *   - Every call returns a uw_status; nothing is thrown across the ABI.  On an
+ *     error, uw_last_error() returns a message for the calling thread.
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary process memory.  The caller owns every buffer it
+ *     passes (weights, blob, X, Y, workspace); the library owns only what a
+ *     uw_matrix holds.
+ *   - Device work is enqueued on the given stream (NULL = legacy default
+ *     stream) and is asynchronous unless stated otherwise.  No entry point
+ *     falls back to the CPU: without a CUDA device they return UW_ERR_CUDA.
+ *   - Shapes: W is [N, K] row-major with K % 64 == 0 (a block is 64 weights of
+ *     one row); X is [B, K] row-major bf16; Y is [B, N] row-major.  Device
+ *     pointers to X, Y and workspaces must be 16-byte aligned.
+ *   - Errors found by device kernels (a Huffman stream that overruns its
+ *     chunk) are latched in a per-matrix status word and reported by uw_check
+ *     and by the next uw_decode / uw_matmul on that matrix.
+ */
+#ifndef UW_H
+#define UW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *uw_stream;
+
+typedef enum {
+    UW_OK = 0,
+    UW_ERR_INVALID_ARG = 1,   /* null pointer, misaligned pointer, bad option value */
+    UW_ERR_SHAPE = 2,         /* K % 64 != 0, negative sizes, B < 0, size overflow */
+    UW_ERR_UNSUPPORTED = 3,   /* strategy not available for this matrix / batch */
+    UW_ERR_CORRUPT = 4,       /* blob failed validation, or a device decoder found a bad stream */
+    UW_ERR_NO_MEMORY = 5,     /* host or device allocation failed */
+    UW_ERR_WORKSPACE = 6,     /* workspace smaller than uw_workspace_size reports */
+    UW_ERR_CUDA = 7,          /* a CUDA runtime call failed (message in uw_last_error) */
+    UW_ERR_TIMEOUT = 8,       /* a bounded device wait expired */
+    UW_ERR_BUFFER_TOO_SMALL = 9 /* host output buffer too small; required size returned */
+} uw_status;
+
+typedef enum { UW_CODEC_PALETTE = 0, UW_CODEC_HUFFMAN = 1 } uw_codec;
+
+/*
+ * Execution strategies, the four pipelines of the "Unweight" post (section on
+ * the four execution pipelines):
+ *   FULL_DECODE        rebuild the whole BF16 matrix into the workspace, then a
+ *                      plain BF16 GEMV/GEMM (the post uses cuBLAS; here a
+ *                      hand-written kernel).
+ *   EXP_ONLY           a preprocess kernel writes only the exponent bytes into
+ *                      the workspace; the fused kernel joins them with the raw
+ *                      sign+mantissa bytes.
+ *   PALETTE_TRANSCODE  a preprocess kernel turns the Huffman stream into 4-bit
+ *                      palette codes in the workspace; the fused kernel rebuilds
+ *                      BF16 from them.
+ *   DIRECT_PALETTE     no preprocessing: the fused kernel reads resident 4-bit
+ *                      codes (palette codec, or a Huffman matrix loaded with its
+ *                      palette form).
+ *   AUTO               the autotuned choice for (matrix, B), else a default.
+ */
+typedef enum {
+    UW_STRAT_AUTO = 0,
+    UW_STRAT_FULL_DECODE = 1,
+    UW_STRAT_EXP_ONLY = 2,
+    UW_STRAT_PALETTE_TRANSCODE = 3,
+    UW_STRAT_DIRECT_PALETTE = 4
+} uw_strategy;
+
+typedef enum { UW_OUT_F32 = 0, UW_OUT_BF16 = 1 } uw_out_dtype;
+
+/* Matmul kernel families. */
+typedef enum {
+    UW_KERNEL_AUTO = 0,
+    UW_KERNEL_GEMV = 1,      /* CUDA-core GEMV, fp32 FMA, batch groups of up to 8 rows of X */
+    UW_KERNEL_TC = 2         /* tcgen05 tensor-core GEMM, W rebuilt in shared memory, fp32 in TMEM */
+} uw_kernel;
+
+typedef struct {
+    uint32_t codec;          /* uw_codec */
+    uint32_t chunk_weights;  /* Huffman chunk size in weights: multiple of 64, >= 64 (default 256) */
+    uint32_t max_code_len;   /* Huffman length limit, 4..15 (default 12) */
+} uw_encode_opts;
+
+/* One execution plan: what uw_matmul runs for a given (matrix, B). */
+typedef struct {
+    int32_t strategy;        /* uw_strategy, never AUTO inside a stored plan */
+    int32_t kernel;          /* uw_kernel */
+    int32_t split_k;         /* K-splits (>= 1); 0 = kernel's default */
+    int32_t variant;         /* kernel-specific tile / pipeline-depth selector; 0 = default */
+} uw_plan;
+
+typedef struct {
+    int64_t N, K;
+    uint32_t codec;
+    uint32_t n_pal;
+    uint8_t palette[16];
+    uint8_t code_len[16];
+    uint64_t n_blocks, n_verbatim, n_chunks, total_bits;
+    uint64_t blob_bytes;     /* size of the serialized blob */
+    uint64_t device_bytes;   /* device memory held by the uw_matrix */
+    int32_t has_palette_form;/* 4-bit codes resident (DIRECT_PALETTE available) */
+    int32_t chunk_weights, max_code_len;
+} uw_info;
+
+typedef struct uw_matrix uw_matrix;
+
+/*
+ * uw_encode - encode W[N,K] (host bf16 bit patterns, row-major) into a blob.
+ *   Passages: BF16 anatomy (sign+mantissa byte kept raw), exponent statistics
+ *   (top-16 palette), Huffman coding of the exponent byte, verbatim 64-weight
+ *   runs.  Host-only, pure and deterministic: the bytes are a function of
+ *   (W, opts) alone.  opts == NULL means palette codec.
+ *   out == NULL: only *out_size is written (required size).  out != NULL and
+ *   out_cap < required: UW_ERR_BUFFER_TOO_SMALL with *out_size = required.
+ *   Errors: UW_ERR_SHAPE (K % 64, negative sizes), UW_ERR_INVALID_ARG (bad
+ *   options), UW_ERR_UNSUPPORTED (Huffman stream of 2^32 bits or more).
+ */
+uw_status uw_encode(const uint16_t *w_host, int64_t N, int64_t K, const uw_encode_opts *opts,
+                    void *out, size_t out_cap, size_t *out_size);
+
+/*
+ * uw_load - validate a blob fully on the host (magic, version, sizes, section
+ *   bounds and alignment, bitmap/prefix/verbatim consistency, code lengths and
+ *   Kraft sum, chunk offsets) and copy it to device memory owned by the new
+ *   uw_matrix.  want_palette_form != 0 on a Huffman blob also materialises the
+ *   4-bit palette codes on the device (the post's load-time transcode for the
+ *   direct-palette pipeline).  Blocks the host until the upload on `stream` is
+ *   done, so the caller may free `blob` on return.
+ *   Errors: UW_ERR_CORRUPT (validation), UW_ERR_NO_MEMORY, UW_ERR_CUDA.
+ */
+uw_status uw_load(const void *blob, size_t size, int want_palette_form, uw_stream stream, uw_matrix **out);
+
+/*
+ * uw_blob_validate - the host-side checks of uw_load without any device work
+ *   (usable on a machine without a GPU).  info may be NULL.
+ *   Errors: UW_ERR_CORRUPT with the first failed check in uw_last_error().
+ */
+uw_status uw_blob_validate(const void *blob, size_t size, uw_info *info);
+
+/* uw_free - release a uw_matrix and its device memory (synchronises the device first). NULL is a no-op. */
+void uw_free(uw_matrix *m);
+
+/* uw_get_info - header facts and memory footprint of a loaded matrix. */
+uw_status uw_get_info(const uw_matrix *m, uw_info *out);
+
+/*
+ * uw_decode - rebuild W[N,K] bf16 (bit-exact, the post's lossless claim) into
+ *   caller-owned device memory w_dev (N*K*2 bytes, 16-byte aligned).
+ *   Asynchronous on `stream`.  Errors: UW_ERR_INVALID_ARG, UW_ERR_CORRUPT (a
+ *   device error latched by an earlier call), UW_ERR_CUDA.
+ */
+uw_status uw_decode(const uw_matrix *m, uint16_t *w_dev, uw_stream stream);
+
+/*
+ * uw_workspace_size - device workspace bytes uw_matmul needs for (m, B,
+ *   strategy) (AUTO: the plan AUTO would pick).  0 is a valid answer.
+ */
+uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strategy strategy, size_t *bytes);
+
+/*
+ * uw_matmul - Y[B,N] = X[B,K] . W^T with W decoded on-chip (the post's
+ *   reconstructive matmul; fp32 accumulation).  x_dev: [B,K] bf16 device;
+ *   y_dev: [B,N] fp32 or bf16 (RNE) device; workspace: device scratch of at
+ *   least uw_workspace_size bytes (may be NULL if that size is 0).  B == 0 is a
+ *   no-op.  Asynchronous on `stream`.
+ *   Errors: UW_ERR_INVALID_ARG, UW_ERR_SHAPE, UW_ERR_UNSUPPORTED (e.g.
+ *   DIRECT_PALETTE without resident codes), UW_ERR_WORKSPACE, UW_ERR_CORRUPT,
+ *   UW_ERR_CUDA.
+ */
+uw_status uw_matmul(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev, uw_out_dtype out_dtype,
+                    uw_strategy strategy, void *workspace, size_t ws_bytes, uw_stream stream);
+
+/* uw_matmul_plan - as uw_matmul, with an explicit plan (strategy, kernel, split, variant). */
+uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev, uw_out_dtype out_dtype,
+                         const uw_plan *plan, void *workspace, size_t ws_bytes, uw_stream stream);
+
+/* uw_plan_workspace_size - workspace bytes for an explicit plan. */
+uw_status uw_plan_workspace_size(const uw_matrix *m, int64_t B, const uw_plan *plan, size_t *bytes);
+
+/* uw_plan_for - the plan AUTO runs for (m, B): the autotuned entry for B's
+ *   bucket if one exists, else a default rule. */
+uw_status uw_plan_for(const uw_matrix *m, int64_t B, uw_plan *out);
+
+/*
+ * uw_matmul_host - end-to-end form of uw_matmul with HOST X and Y: copies
+ *   x_host ([B,K] bf16) to the device, runs the plan AUTO picks, copies Y back
+ *   into y_host and synchronises `stream` before returning.  workspace must be
+ *   a device buffer of at least uw_host_workspace_size bytes (it also holds
+ *   the device copies of X and Y).  Pinned host memory gives the fastest copies.
+ */
+uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
+                         uw_out_dtype out_dtype, void *workspace, size_t ws_bytes, uw_stream stream);
+uw_status uw_host_workspace_size(const uw_matrix *m, int64_t B, uw_out_dtype out_dtype, size_t *bytes);
+
+/*
+ * uw_autotune - for each batch size in batches[0..n_batches), time the
+ *   candidate plans on this GPU (CUDA events on `stream`, several repetitions,
+ *   median) by coordinate descent over strategy, kernel, split and variant (the
+ *   post's autotuner: measure real throughput, vary one choice at a time until
+ *   nothing improves), and store the fastest in the matrix's tune table, keyed
+ *   by batch bucket.  workspace must hold uw_workspace_size for every candidate
+ *   (uw_autotune_workspace_size).  Synchronous.  Writes scratch outputs only
+ *   into the workspace.
+ */
+uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n_batches, void *workspace, size_t ws_bytes,
+                      uw_stream stream);
+uw_status uw_autotune_workspace_size(const uw_matrix *m, const int64_t *batches, int n_batches, size_t *bytes);
+
+/*
+ * uw_tune_save / uw_tune_load - the tune table as text, one line per batch
+ *   bucket: "B strategy kernel split_k variant us".  save: buf == NULL returns
+ *   the length in *len.  load replaces the table; it rejects malformed lines
+ *   with UW_ERR_INVALID_ARG and leaves the table unchanged.
+ */
+uw_status uw_tune_save(const uw_matrix *m, char *buf, size_t cap, size_t *len);
+uw_status uw_tune_load(uw_matrix *m, const char *text);
+
+/* uw_check - synchronise `stream` and report (then clear) the matrix's device status word. */
+uw_status uw_check(const uw_matrix *m, uw_stream stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *uw_status_string(uw_status s);
+
+/* Last error message of the calling thread ("" if none). */
+const char *uw_last_error(void);
+
+/* Library build string (version, target architecture). */
+const char *uw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UW_H */

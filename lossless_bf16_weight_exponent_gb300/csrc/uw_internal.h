@@ -1,0 +1,93 @@
+// uw_internal.h - declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/uw.h"
+
+namespace uw {
+
+constexpr int kBlock = 64;              // weights per verbatim decision
+constexpr uint64_t kAlign = 256;        // blob section alignment
+constexpr int kMaxBatchBuckets = 32;
+
+enum Section { S_SM = 0, S_BITMAP, S_PREFIX, S_VERB, S_IDX, S_CHUNK, S_BITS, S_COUNT };
+
+struct BlobHeader {
+    int64_t N = 0, K = 0;
+    uint32_t codec = 0, block = 64, chunk = 0, max_len = 0;
+    uint32_t n_pal = 0;
+    uint8_t palette[16] = {0};
+    uint8_t code_len[16] = {0};
+    uint64_t n_blocks = 0, n_verbatim = 0, n_chunks = 0, total_bits = 0, blob_bytes = 0;
+    uint64_t off[S_COUNT] = {0}, len[S_COUNT] = {0};
+};
+
+// error reporting (thread-local message)
+uw_status fail(uw_status s, const char *fmt, ...);
+void clear_error();
+
+// host codec (uw_host.cpp)
+uw_status parse_and_validate(const uint8_t *blob, size_t size, BlobHeader *h, bool deep);
+void canonical_codes(const uint8_t *lens, uint32_t *codes);
+// Decode table for a canonical code: entry[v] for every max_len-bit prefix v is
+// (symbol << 4) | length, 0 where no code matches.
+void build_decode_table(const uint8_t *lens, int max_len, std::vector<uint8_t> &table);
+
+// --------------------------------------------------------------------------------------------
+// Device view of a loaded matrix (plain pointers, passed by value to kernels).
+struct DevView {
+    int64_t N, K;
+    uint64_t n_blocks, n_chunks;
+    uint32_t chunk, max_len;
+    uint32_t n_pal;
+    uint8_t palette[16];
+    const uint8_t *sm;        // [N*K] sign<<7 | mantissa
+    const uint32_t *bitmap;   // [ceil(n_blocks/32)] verbatim flags, LSB first
+    const uint32_t *prefix;   // [ceil(n_blocks/32)] verbatim blocks before each word
+    const uint8_t *verb_exp;  // [n_verbatim*64] exponents of verbatim blocks
+    const uint8_t *codes;     // [N*K/2] 4-bit palette codes (resident form) or nullptr
+    const uint32_t *chunk_off;// [n_chunks+1] bit offsets (Huffman)
+    const uint32_t *bits;     // Huffman bit string, MSB-first u32 words, + guard words
+    const uint8_t *dtab;      // [1 << max_len] decode table (Huffman)
+    int *status;              // device status word (0 = ok)
+};
+
+// Device-side status values written by kernels.
+enum DevStatus { DEV_OK = 0, DEV_CORRUPT = 1, DEV_TIMEOUT = 2 };
+
+// Weight-stream formats consumed by the matmul kernels.
+enum WFormat { FMT_PAL = 0, FMT_EXP = 1, FMT_BF16 = 2 };
+// Outputs of the preprocess / decode kernels.
+enum DecOut { DEC_BF16 = 0, DEC_EXP = 1, DEC_CODES = 2 };
+
+// Operand description for a matmul launch.
+struct WOperand {
+    int fmt;                  // WFormat
+    const uint8_t *sm;        // FMT_PAL / FMT_EXP
+    const uint8_t *codes;     // FMT_PAL
+    const uint8_t *exps;      // FMT_EXP: [N*K] exponent bytes
+    const uint16_t *w;        // FMT_BF16: [N*K]
+    const uint32_t *bitmap, *prefix;
+    const uint8_t *verb_exp;  // FMT_PAL verbatim handling
+    uint8_t palette[16];
+    int64_t N, K;
+};
+
+// kernel launchers (k_decode.cu, k_gemv.cu, k_tc.cu); return cudaError_t as int
+int launch_decode_palette(const DevView &v, int out_kind, void *out, void *stream);
+int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream);
+int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k,
+                int variant, float *acc_ws, void *stream);
+int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
+int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
+              float *acc_ws, void *stream);
+bool tc_supported(const WOperand &w, int64_t B, int variant);
+int gemv_default_split(const WOperand &w, int64_t B);
+int tc_default_split(const WOperand &w, int64_t B, int variant);
+int num_sms();
+
+}  // namespace uw
