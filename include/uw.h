@@ -205,6 +205,30 @@ uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, int64_t B, 
 uw_status uw_host_workspace_size(const uw_matrix *m, int64_t B, uw_out_dtype out_dtype, size_t *bytes);
 
 /*
+ * uw_matmul_noalloc - uw_matmul with the palette-transcode pipeline
+ *   (UW_STRAT_PALETTE_TRANSCODE on the GEMV kernel) that allocates nothing and
+ *   takes no workspace.  The Unweight post has no counterpart to this entry
+ *   point; it exists for callers that cannot call cudaMalloc - an engine whose
+ *   allocator reserved all device memory at start-up, or a latency-critical
+ *   path that must not take the device synchronisation cudaMalloc / cudaFree may
+ *   imply.  Its scratch (the transcoded 4-bit codes, plus the fp32 accumulator a
+ *   K-split may need) is a library-owned static device array of 36 MiB, held on
+ *   every GPU that loads the library until the process exits.
+ *   m must be a Huffman-coded matrix; x_dev, y_dev, B and out_dtype are as in
+ *   uw_matmul.  The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before
+ *   any stream capture.  All calls share the one array and it keeps the last
+ *   call's contents (the accumulator is cleared on the stream before each use):
+ *   calls whose GPU work overlaps (different streams, or different threads
+ *   without ordering) race on it.
+ *   Errors: UW_ERR_WORKSPACE when N*K/2 plus B*N*4 (each rounded up to 256
+ *   bytes, with 64 bytes of padding on the codes) exceeds the 36 MiB array;
+ *   UW_ERR_UNSUPPORTED for a palette-codec matrix; otherwise as uw_matmul.
+ */
+uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev, uw_out_dtype out_dtype,
+                            uw_stream stream);
+
+/*
  * uw_autotune - for each batch size in batches[0..n_batches), time the
  *   candidate plans on this GPU (CUDA events on `stream`, several repetitions,
  *   median) by coordinate descent over strategy, kernel, split and variant (the

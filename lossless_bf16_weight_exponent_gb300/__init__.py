@@ -87,6 +87,7 @@ _SIGS = {
     "uw_tune_save": [_VP, ctypes.c_char_p, _SZ, ctypes.POINTER(_SZ)],
     "uw_tune_load": [_VP, ctypes.c_char_p],
     "uw_check": [_VP, _VP],
+    "uw_matmul_noalloc": [_VP, _VP, _I64, _VP, _INT, _VP],
     "uw_status_string": [_INT],
     "uw_last_error": [],
     "uw_version": [],
@@ -246,6 +247,9 @@ class Matrix:
 
     def tune_load(self, text: str):
         _check(lib().uw_tune_load(self._h, text.encode()), "uw_tune_load")
+
+    def matmul_noalloc(self, x, B: int, y, out_dtype: int = OUT_F32, stream=None):
+        _check(lib().uw_matmul_noalloc(self._h, _ptr(x), B, _ptr(y), out_dtype, _stream(stream)), "uw_matmul_noalloc")
 
     def check(self, stream=None):
         _check(lib().uw_check(self._h, _stream(stream)), "uw_check")

@@ -1,0 +1,87 @@
+// uw_noalloc.cu - the palette-transcode matmul with its scratch in a static device array.
+//
+// Some callers cannot call cudaMalloc: an inference engine whose allocator has
+// reserved all of the device's memory at start-up (every later cudaMalloc fails
+// or fragments its pool), or code on a latency-critical path that must not take
+// the device-wide synchronisation cudaMalloc / cudaFree may imply.  For them,
+// uw_matmul_noalloc runs the same kernels as uw_matmul with the palette-transcode
+// pipeline, but its scratch (the transcoded 4-bit codes and, when the K-split
+// needs one, the fp32 accumulator) lives in the array below, which the driver
+// places on every device that loads this library and keeps there until the
+// process exits.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "uw_internal.h"
+
+// Library-owned scratch: UW_NOALLOC_SCRATCH_BYTES (36 MiB) per device.
+#define UW_NOALLOC_SCRATCH_BYTES (36u * 1024u * 1024u)
+static __device__ __align__(256) uint8_t g_noalloc_scratch[UW_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+uw_status scratch_address(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return uw::fail(UW_ERR_CUDA, "uw_matmul_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return uw::fail(UW_ERR_UNSUPPORTED, "uw_matmul_noalloc: device %d", dev);
+    std::lock_guard<std::mutex> g(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return uw::fail(UW_ERR_CUDA, "uw_matmul_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return UW_OK;
+}
+
+uint64_t round_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev,
+                                       uw_out_dtype out_dtype, uw_stream stream)
+{
+    uw::clear_error();
+    if (!m) return uw::fail(UW_ERR_INVALID_ARG, "uw_matmul_noalloc: NULL matrix");
+    uw_info info;
+    uw_status s = uw_get_info(m, &info);
+    if (s != UW_OK) return s;
+    if (info.codec != UW_CODEC_HUFFMAN)
+        return uw::fail(UW_ERR_UNSUPPORTED, "uw_matmul_noalloc: needs a Huffman-coded matrix (palette transcode)");
+    if (B < 0) return uw::fail(UW_ERR_SHAPE, "uw_matmul_noalloc: B < 0");
+    if (B == 0 || info.N == 0) return UW_OK;
+    if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15) || ((uintptr_t)y_dev & 15))
+        return uw::fail(UW_ERR_INVALID_ARG, "uw_matmul_noalloc: X/Y NULL or not 16-byte aligned");
+    if (out_dtype != UW_OUT_F32 && out_dtype != UW_OUT_BF16)
+        return uw::fail(UW_ERR_INVALID_ARG, "uw_matmul_noalloc: bad output dtype");
+    const uint64_t n = (uint64_t)info.N * (uint64_t)info.K;
+    const uint64_t codes_bytes = round_up(n / 2 + 64, 256);
+    const uint64_t acc_bytes = round_up((uint64_t)B * (uint64_t)info.N * 4, 256);
+    if (codes_bytes + acc_bytes > UW_NOALLOC_SCRATCH_BYTES)
+        return uw::fail(UW_ERR_WORKSPACE,
+                        "uw_matmul_noalloc: needs %llu scratch bytes (4-bit codes %llu + accumulator %llu), "
+                        "the static scratch holds %u",
+                        (unsigned long long)(codes_bytes + acc_bytes), (unsigned long long)codes_bytes,
+                        (unsigned long long)acc_bytes, UW_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    s = scratch_address(&scratch);
+    if (s != UW_OK) return s;
+    // Same plan as uw_matmul with UW_STRAT_PALETTE_TRANSCODE on the GEMV kernel, workspace = the static array.
+    uw_plan plan{};
+    plan.strategy = UW_STRAT_PALETTE_TRANSCODE;
+    plan.kernel = UW_KERNEL_GEMV;
+    return uw_matmul_plan(m, x_dev, B, y_dev, out_dtype, &plan, scratch, UW_NOALLOC_SCRATCH_BYTES, stream);
+}
