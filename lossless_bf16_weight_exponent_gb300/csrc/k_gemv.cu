@@ -82,50 +82,73 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// sm byte i of a 16-byte group placed in bits 31..16 twice, masked to sign | mantissa positions
-__device__ __forceinline__ uint32_t sm_bits(const uint4 &s, int i)
+// bf16x2 from 4 sign+mantissa bytes S and 4 exponent bytes E: returns the pairs (w1:w0) and (w3:w2).
+__device__ __forceinline__ void pairs_from_exps(uint32_t S, uint32_t E, uint32_t &p01, uint32_t &p23)
 {
-    const uint32_t word = word_of(s, i >> 2);
-    const uint32_t b = i & 3;
-    return __byte_perm(word, 0u, (b << 12) | (b << 8) | 0x44u) & 0x807F0000u;
+    const uint32_t hi = (S & 0x80808080u) | ((E >> 1) & 0x7F7F7F7Fu);   // sign | exponent bits 7..1
+    const uint32_t lo = (S & 0x7F7F7F7Fu) | ((E << 7) & 0x80808080u);   // exponent bit 0 | mantissa
+    p01 = __byte_perm(lo, hi, 0x5140u);
+    p23 = __byte_perm(lo, hi, 0x7362u);
+}
+
+// fp32 values of a bf16x2 pair: low half then high half
+__device__ __forceinline__ void unpack2(uint32_t p, float &f0, float &f1)
+{
+    f0 = __uint_as_float(p * 65536u);  // a multiply keeps this shift off the integer ALU pipe
+    f1 = __uint_as_float(p & 0xFFFF0000u);
+}
+
+// Palette pair table: for a code byte b (codes c0 = b & 15, c1 = b >> 4) the exponent fields of a bf16x2
+// pair, (pal[c1] << 23) | (pal[c0] << 7).  Replicated for each of the 32 lanes at byte offset b*128 + 4*lane,
+// so a warp's 32 lookups always touch 32 different banks.
+constexpr int kPairTableBytes = 256 * 32 * 4;
+
+__device__ __forceinline__ uint32_t pair_exp(const uint8_t *tab_lane, uint32_t C, int j)
+{
+    // byte j of C, times 128
+    const uint32_t off = (j == 0 ? (C << 7) : (C >> (8 * j - 7))) & 0x7F80u;
+    return *(const uint32_t *)(tab_lane + off);
 }
 
 template <int FMT>
-__device__ __forceinline__ void rebuild16(const WOperand &w, uint64_t off, const Raw<FMT> &r, const uint32_t *e23,
+__device__ __forceinline__ void rebuild16(const WOperand &w, uint64_t off, const Raw<FMT> &r, const uint8_t *tab_lane,
                                           float *f)
 {
     if constexpr (FMT == FMT_PAL) {
         const uint64_t b = off >> 6;
-        if ((r.bw >> (b & 31)) & 1u) {
+        if (__builtin_expect((r.bw >> (b & 31)) & 1u, 0)) {
             const uint64_t vi = __ldg(w.prefix + (b >> 5)) + __popc(r.bw & ((1u << (b & 31)) - 1u));
             const uint4 ev = __ldg((const uint4 *)(w.verb_exp + vi * 64 + (off & 63)));
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint32_t e = (word_of(ev, i >> 2) >> (8 * (i & 3))) & 0xFFu;
-                f[i] = __uint_as_float(sm_bits(r.s, i) | (e << 23));
+            for (int q = 0; q < 4; q++) {
+                uint32_t p01, p23;
+                pairs_from_exps(word_of(r.s, q), word_of(ev, q), p01, p23);
+                unpack2(p01, f[4 * q], f[4 * q + 1]);
+                unpack2(p23, f[4 * q + 2], f[4 * q + 3]);
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint32_t code = ((i < 8 ? r.c.x : r.c.y) >> (4 * (i & 7))) & 15u;
-                f[i] = __uint_as_float(sm_bits(r.s, i) | e23[code]);
+            for (int q = 0; q < 4; q++) {
+                const uint32_t S = word_of(r.s, q);
+                const uint32_t C = q < 2 ? r.c.x : r.c.y;
+                const int j = 2 * (q & 1);
+                const uint32_t p01 = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab_lane, C, j);
+                const uint32_t p23 = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab_lane, C, j + 1);
+                unpack2(p01, f[4 * q], f[4 * q + 1]);
+                unpack2(p23, f[4 * q + 2], f[4 * q + 3]);
             }
         }
     } else if constexpr (FMT == FMT_EXP) {
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const uint32_t eword = word_of(r.e, i >> 2);
-            const uint32_t b = i & 3;
-            const uint32_t e_hi = __byte_perm(eword, 0u, 0x0444u | (b << 12));  // exponent byte in bits 31..24
-            f[i] = __uint_as_float(sm_bits(r.s, i) | (e_hi >> 1));
+        for (int q = 0; q < 4; q++) {
+            uint32_t p01, p23;
+            pairs_from_exps(word_of(r.s, q), word_of(r.e, q), p01, p23);
+            unpack2(p01, f[4 * q], f[4 * q + 1]);
+            unpack2(p23, f[4 * q + 2], f[4 * q + 3]);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const uint32_t word = word_of(i < 4 ? r.lo : r.hi, i & 3);
-            f[2 * i] = __uint_as_float(word << 16);
-            f[2 * i + 1] = __uint_as_float(word & 0xFFFF0000u);
-        }
+        for (int i = 0; i < 8; i++) unpack2(word_of(i < 4 ? r.lo : r.hi, i & 3), f[2 * i], f[2 * i + 1]);
     }
 }
 
@@ -143,13 +166,18 @@ template <int NB, int FMT>
 __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a)
 {
     extern __shared__ float4 xs4[];
-    __shared__ uint32_t e23[16];
     const int64_t N = a.w.N, K = a.w.K;
     const int64_t k0 = (int64_t)blockIdx.y * a.ks;
     const int klen = (int)(a.ks < K - k0 ? a.ks : K - k0);
     const int ksp = (int)a.ks;  // row pitch of the X slice (floats)
     const int64_t b0 = (int64_t)blockIdx.z * NB;
-    if (threadIdx.x < 16) e23[threadIdx.x] = (uint32_t)a.w.palette[threadIdx.x] << 23;
+    uint8_t *tab = (uint8_t *)(xs4 + NB * (ksp / 4));
+    if constexpr (FMT == FMT_PAL) {
+        for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
+            const int b = i >> 5;
+            ((uint32_t *)tab)[i] = ((uint32_t)a.w.palette[b >> 4] << 23) | ((uint32_t)a.w.palette[b & 15] << 7);
+        }
+    }
 
     // X slice -> fp32, swizzled
     const int chunks = klen / 4;
@@ -166,6 +194,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a)
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint8_t *tab_lane = tab + 4 * lane;
     const int64_t row0 = (int64_t)blockIdx.x * 16 + warp * 2;
     const bool ok0 = row0 < N, ok1 = row0 + 1 < N;
     const uint64_t base0 = (uint64_t)row0 * K + k0, base1 = base0 + K;
@@ -188,12 +217,12 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a)
             if (ok1) load_raw<FMT>(a.w, base1 + kn, nxt1);
         }
         float w0[16], w1[16];
-        if (ok0) rebuild16<FMT>(a.w, base0 + kk, cur0, e23, w0);
+        if (ok0) rebuild16<FMT>(a.w, base0 + kk, cur0, tab_lane, w0);
         else {
 #pragma unroll
             for (int i = 0; i < 16; i++) w0[i] = 0.f;
         }
-        if (ok1) rebuild16<FMT>(a.w, base1 + kk, cur1, e23, w1);
+        if (ok1) rebuild16<FMT>(a.w, base1 + kk, cur1, tab_lane, w1);
         else {
 #pragma unroll
             for (int i = 0; i < 16; i++) w1[i] = 0.f;
@@ -245,6 +274,7 @@ __global__ void finalize_kernel(const float *acc, void *y, int64_t count, int ou
 }
 
 constexpr int64_t kMaxSlice = 160 * 1024;  // bytes of X slice per CTA
+constexpr int kMaxSmem = (int)kMaxSlice + kPairTableBytes;
 
 template <int NB, int FMT>
 cudaError_t launch_nb(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t st)
@@ -252,7 +282,7 @@ cudaError_t launch_nb(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t st
     static bool attr_set = false;  // set once, outside any stream capture (first call is never captured)
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NB, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kMaxSlice);
+                                             kMaxSmem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -289,9 +319,13 @@ int gemv_default_split(const WOperand &w, int64_t B)
 int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
                 float *acc_ws, void *stream)
 {
-    (void)variant;
     if (B <= 0 || w.N == 0) return cudaSuccess;
     cudaStream_t st = (cudaStream_t)stream;
+    if (variant != 1 && w.K > 0) {
+        // the default (variant 0) falls back to the one-CTA-per-SM shape when two CTAs do not fit
+        const int v = (variant == 0 && !gemv_tma_supported(w, B, 0)) ? 2 : variant;
+        if (gemv_tma_supported(w, B, v)) return launch_gemv_tma(w, x, B, y, out_bf16, split_k, v, acc_ws, w.status, stream);
+    }
     const int nb = batch_group(B);
     if (w.K == 0) {
         size_t bytes = (size_t)B * w.N * (out_bf16 ? 2 : 4);
@@ -311,7 +345,7 @@ int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int ou
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)((w.N + 15) / 16), (unsigned)nsplit, (unsigned)((B + nb - 1) / nb));
-    const size_t smem = (size_t)nb * ks * 4;
+    const size_t smem = (size_t)nb * ks * 4 + (w.fmt == FMT_PAL ? kPairTableBytes : 0);
     cudaError_t e;
     if (w.fmt == FMT_PAL) e = launch_fmt<FMT_PAL>(nb, a, grid, smem, st);
     else if (w.fmt == FMT_EXP) e = launch_fmt<FMT_EXP>(nb, a, grid, smem, st);

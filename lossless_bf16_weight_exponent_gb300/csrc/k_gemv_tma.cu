@@ -1,0 +1,515 @@
+// k_gemv_tma.cu - persistent fused reconstruct + GEMV fed by bulk-async copies (sm_103a), B <= 2.
+//
+// Cloudflare blog "Unweight", section on the reconstructive matmul: a producer
+// moves compressed inputs from HBM into a circular shared-memory buffer with the
+// copy engine and runs ahead of the consumers; consumers rebuild BF16 from the
+// exponent data and the sign+mantissa bytes and feed the product at once.  The
+// H100 kernel in the post feeds WGMMA; at batch 1-2 this contraction is a
+// matrix-vector product bound by HBM, so the consumers here use fp32 FMAs.
+//
+// One CTA per SM owns a contiguous range of rows.  Warp 0 (one elected thread)
+// issues cp.async.bulk copies of whole row slices - sign+mantissa bytes and the
+// 4-bit codes (or exponent bytes, or plain bf16) - into a ring of S stages, each
+// stage RS rows, with an mbarrier per stage for "full" (transaction bytes) and
+// one for "empty" (one arrive per consumer warp).  Consumer warp c handles row
+// slot c / WK of a stage and the c % WK-th piece of the K-slice: lane l owns the
+// weights k = piece*32*LW + 16*l + 512*g (g < LW/16), so its X values stay in
+// registers for the whole kernel and its 16-byte shared loads are bank-conflict
+// free.  Row partial sums meet in shared memory (atomic adds) and are written
+// once at the end.  Every mbarrier wait is bounded by a global-timer limit; on
+// expiry the kernel latches DEV_TIMEOUT, drains the copies it issued and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "uw_internal.h"
+
+namespace uw {
+
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait: far above any legitimate stall
+
+struct TmaArgs {
+    WOperand w;
+    const uint16_t *x;
+    int64_t B;
+    void *y;
+    float *acc;
+    int out_bf16;
+    int nsplit;
+    int ks;          // K-slice length (multiple of 64)
+    int rs;          // rows per stage
+    int stages;      // ring depth
+    int wk;          // consumer warps per row
+    int stage_bytes; // bytes of one stage
+    int rows_cta;    // max rows owned by one CTA
+    int bm_words;    // max verbatim-bitmap words of one CTA's rows
+    int vcap;        // verbatim blocks of the CTA's rows staged in shared memory (beyond: global loads)
+    int w_from_prev; // the weight stream is written by the preceding kernel (a preprocess workspace)
+    int *status;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the barrier's phase with this parity completes; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// acc += w * x for both halves of a bf16x2 pair of weights and of activations: BF16 products are exact in
+// fp32, so this equals two fp32 FMAs on the widened values, without widening them first.
+__device__ __forceinline__ float fma2_bf16(uint32_t w2, uint32_t x2, float acc)
+{
+    asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+        " fma.rn.f32.bf16 %0, wl, xl, %0;\n fma.rn.f32.bf16 %0, wh, xh, %0;\n}\n"
+        : "+f"(acc)
+        : "r"(w2), "r"(x2));
+    return acc;
+}
+
+__device__ __forceinline__ void pairs_from_exps(uint32_t S, uint32_t E, uint32_t &p01, uint32_t &p23)
+{
+    const uint32_t hi = (S & 0x80808080u) | ((E >> 1) & 0x7F7F7F7Fu);
+    const uint32_t lo = (S & 0x7F7F7F7Fu) | ((E << 7) & 0x80808080u);
+    p01 = __byte_perm(lo, hi, 0x5140u);
+    p23 = __byte_perm(lo, hi, 0x7362u);
+}
+
+// Palette pair table: for a code byte b (codes c0 = b & 15, c1 = b >> 4) the exponent fields of the bf16x2
+// pair, (pal[c1] << 23) | (pal[c0] << 7), stored for each lane at byte offset 256*b + 4*lane.  A warp's 32
+// lookups always hit 32 different banks, and the offset of byte j of a code word C is a single byte
+// permute, [0, 0, byte j of C, 4*lane] (bytes 128..255 of each entry row are unused).
+constexpr int kTableBytes = 256 * 256;
+
+__device__ __forceinline__ uint32_t pair_exp(const uint8_t *tab, uint32_t C, uint32_t lane4, int j)
+{
+    return *(const uint32_t *)(tab + __byte_perm(C, lane4, 0x5504u | (uint32_t)(j << 4)));
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// bytes per weight in a stage, per format
+template <int FMT> struct Fmt;
+template <> struct Fmt<FMT_PAL> { static constexpr int num = 3, den = 2; };   // sm + 4-bit code
+template <> struct Fmt<FMT_EXP> { static constexpr int num = 2, den = 1; };   // sm + exponent byte
+template <> struct Fmt<FMT_BF16> { static constexpr int num = 2, den = 1; };  // bf16
+
+template <int NB, int LW, int FMT>
+__global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int G = LW / 16;
+    const int64_t N = a.w.N, K = a.w.K;
+    const int64_t k0 = (int64_t)blockIdx.y * a.ks;
+    const int klen = (int)min((int64_t)a.ks, K - k0);
+    const int64_t b0 = (int64_t)blockIdx.z * NB;
+    // rows of this CTA: balanced partition of N over gridDim.x
+    const int64_t r0 = N * blockIdx.x / gridDim.x, r1 = N * (blockIdx.x + 1) / gridDim.x;
+    const int nrows = (int)(r1 - r0);
+    const int n_stages = (nrows + a.rs - 1) / a.rs;
+    // verbatim bitmap words covering the CTA's rows
+    const uint64_t wb0 = ((uint64_t)r0 * K / 64) >> 5;
+    const int n_bw = nrows ? (int)((((uint64_t)r1 * K / 64 - 1) >> 5) - wb0 + 1) : 0;
+
+    uint8_t *tab = smem;                                              // pair table (FMT_PAL)
+    uint64_t *full = (uint64_t *)(smem + kTableBytes);               // [stages]
+    uint64_t *empty = full + a.stages;                                // [stages]
+    float *part = (float *)(smem + kTableBytes + 1024);               // [rows_cta][NB]
+    const int part_bytes = (a.rows_cta * NB * 4 + 1023) / 1024 * 1024;
+    const int bm_bytes = (a.bm_words * 4 + 1023) / 1024 * 1024;
+    uint32_t *bm = (uint32_t *)(smem + kTableBytes + 1024 + part_bytes);              // [bm_words] bitmap
+    uint32_t *pf = (uint32_t *)(smem + kTableBytes + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
+    uint8_t *vx = smem + kTableBytes + 1024 + part_bytes + 2 * bm_bytes;              // [vcap][64] verbatim exps
+    uint8_t *ring = vx + (size_t)a.vcap * 64;
+    uint64_t *vfull = empty + a.stages;                                                // verbatim staging barrier
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = a.rs * a.wk;  // consumer warps
+    if (FMT == FMT_PAL) {
+        // consecutive threads fill consecutive 16-byte chunks: bank-conflict-free stores
+        for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
+            const int b = i >> 3, q = i & 7;
+            const uint32_t v = ((uint32_t)a.w.palette[b >> 4] << 23) | ((uint32_t)a.w.palette[b & 15] << 7);
+            *(uint4 *)(tab + 256 * b + 16 * q) = make_uint4(v, v, v, v);
+        }
+        for (int i = threadIdx.x; i < n_bw; i += blockDim.x) {
+            bm[i] = __ldg(a.w.bitmap + wb0 + i);
+            pf[i] = __ldg(a.w.prefix + wb0 + i);
+        }
+    }
+    for (int i = threadIdx.x; i < a.rows_cta * NB; i += blockDim.x) part[i] = 0.f;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C);
+        }
+        mbar_init(vfull, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // verbatim blocks of the CTA's rows form one contiguous run of the verbatim stream: [v_begin, v_end)
+    uint64_t v_begin = 0;
+    int v_staged = 0;
+    if (FMT == FMT_PAL && nrows) {
+        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
+        const uint32_t w0 = bm[0];
+        v_begin = pf[0] + __popc(w0 & ((1u << (fb & 31)) - 1u));
+        const uint64_t lw = lb >> 5;
+        uint64_t v_end;
+        if (lw - wb0 < (uint64_t)n_bw) v_end = pf[lw - wb0] + __popc(bm[lw - wb0] & ((1u << (lb & 31)) - 1u));
+        else v_end = pf[n_bw - 1] + __popc(bm[n_bw - 1]);
+        v_staged = (int)(v_end - v_begin < (uint64_t)a.vcap ? v_end - v_begin : (uint64_t)a.vcap);
+    }
+    // a dependent launch may start its prologue and stream its own weights from here on
+    grid_launch_dependents();
+
+    const uint32_t wbytes = (uint32_t)((int64_t)klen * Fmt<FMT>::num / Fmt<FMT>::den);  // per row
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
+            if (FMT == FMT_PAL) {
+                mbar_arrive_expect_tx(vfull, (uint32_t)v_staged * 64);
+                if (v_staged) bulk_g2s(vx, a.w.verb_exp + v_begin * 64, (uint32_t)v_staged * 64, vfull);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < n_stages && ok; i++) {
+                const int slot = i % a.stages;
+                if (i >= a.stages && !mbar_wait(&empty[slot], ((i / a.stages) - 1) & 1)) { ok = false; break; }
+                const int64_t g0 = r0 + (int64_t)i * a.rs;
+                const int nr = (int)min((int64_t)a.rs, r1 - g0);
+                uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[slot], wbytes * nr);
+                for (int r = 0; r < nr; r++) {
+                    const uint64_t off = (uint64_t)(g0 + r) * K + k0;
+                    if (FMT == FMT_PAL) {
+                        bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
+                        bulk_g2s(st + a.rs * klen + r * (klen / 2), a.w.codes + off / 2, klen / 2, &full[slot]);
+                    } else if (FMT == FMT_EXP) {
+                        bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
+                        bulk_g2s(st + a.rs * klen + r * klen, a.w.exps + off, klen, &full[slot]);
+                    } else {
+                        bulk_g2s(st + r * 2 * klen, a.w.w + off, 2 * klen, &full[slot]);
+                    }
+                }
+                issued = i + 1;
+            }
+            if (!ok) {
+                atomicExch(a.status, (int)DEV_TIMEOUT);
+                if (FMT == FMT_PAL) mbar_wait(vfull, 0);
+                // drain: every issued stage's copies must land before the CTA may exit
+                for (int i = max(0, issued - a.stages); i < issued; i++) mbar_wait(&full[i % a.stages], (i / a.stages) & 1);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int c = warp - 1;
+    const int slot_row = c / a.wk, piece = c % a.wk;
+    const int kbase = piece * 32 * LW + 16 * lane;
+    const uint32_t lane4 = 4u * (uint32_t)lane;
+    grid_dependency_wait();   // X (and Y, written below) belong to the stream order after the preceding kernel
+    uint32_t xr[NB][LW / 2];  // bf16x2 activations of the lane's weights
+#pragma unroll
+    for (int j = 0; j < NB; j++)
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            const int kk = kbase + 512 * g;
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            if (kk < klen && b0 + j < a.B) {
+                const uint4 *src = (const uint4 *)(a.x + (b0 + j) * K + k0 + kk);
+                lo = __ldg(src);
+                hi = __ldg(src + 1);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                xr[j][8 * g + q] = word_of(lo, q);
+                xr[j][8 * g + 4 + q] = word_of(hi, q);
+            }
+        }
+    // block index of the lane's first group in the first stage, relative to the CTA's first bitmap word
+    const uint64_t blk_lane0 = (((uint64_t)(r0 + slot_row) * K + k0 + kbase) >> 6) - wb0 * 32;
+    const uint64_t blk_stage = (uint64_t)a.rs * K / 64;
+    bool ok = true;
+    if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
+    for (int i = 0; i < n_stages && ok; i++) {
+        const int slot = i % a.stages;
+        if (!mbar_wait(&full[slot], (i / a.stages) & 1)) { ok = false; break; }
+        const int64_t g0 = r0 + (int64_t)i * a.rs;
+        const int64_t row = g0 + slot_row;
+        if (row < r1) {
+            const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+            float acc0[NB], acc1[NB];
+#pragma unroll
+            for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                const int kk = kbase + 512 * g;
+                if (kk < klen) {
+                    uint32_t pw[8];  // 8 bf16x2 pairs of weights
+                    if (FMT == FMT_PAL) {
+                        const uint4 s = *(const uint4 *)(st + slot_row * klen + kk);
+                        const uint2 cc = *(const uint2 *)(st + a.rs * klen + slot_row * (klen / 2) + kk / 2);
+                        const uint32_t bl = (uint32_t)(blk_lane0 + i * blk_stage) + (uint32_t)(8 * g);  // 512 weights = 8 blocks
+                        const uint32_t bw = bm[bl >> 5];
+                        if (__builtin_expect((bw >> (bl & 31)) & 1u, 0)) {
+                            const uint64_t vi = pf[bl >> 5] + __popc(bw & ((1u << (bl & 31)) - 1u));
+                            const uint64_t vl = vi - v_begin;
+                            const int within = kk & 63;
+                            const uint4 ev = vl < (uint64_t)v_staged
+                                                 ? *(const uint4 *)(vx + vl * 64 + within)
+                                                 : __ldg((const uint4 *)(a.w.verb_exp + vi * 64 + within));
+#pragma unroll
+                            for (int q = 0; q < 4; q++) pairs_from_exps(word_of(s, q), word_of(ev, q), pw[2 * q], pw[2 * q + 1]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                const uint32_t S = word_of(s, q);
+                                const uint32_t Cw = q < 2 ? cc.x : cc.y;
+                                const int jb = 2 * (q & 1);
+                                pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab, Cw, lane4, jb);
+                                pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab, Cw, lane4, jb + 1);
+                            }
+                        }
+                    } else if (FMT == FMT_EXP) {
+                        const uint4 s = *(const uint4 *)(st + slot_row * klen + kk);
+                        const uint4 e = *(const uint4 *)(st + a.rs * klen + slot_row * klen + kk);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) pairs_from_exps(word_of(s, q), word_of(e, q), pw[2 * q], pw[2 * q + 1]);
+                    } else {
+                        const uint4 lo = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk);
+                        const uint4 hi = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk + 16);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) { pw[q] = word_of(lo, q); pw[4 + q] = word_of(hi, q); }
+                    }
+#pragma unroll
+                    for (int j = 0; j < NB; j++)
+#pragma unroll
+                        for (int t = 0; t < 8; t += 2) {
+                            acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
+                            acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; j++) {
+                float v = acc0[j] + acc1[j];
+#pragma unroll
+                for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                if (lane == 0) atomicAdd(&part[(row - r0) * NB + j], v);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
+    asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");
+    // write the CTA's rows
+    const int tid = threadIdx.x - 32;
+    for (int i = tid; i < nrows * NB; i += C * 32) {
+        const int rl = i / NB, j = i - rl * NB;
+        if (b0 + j >= a.B) continue;
+        const int64_t o = (b0 + j) * N + r0 + rl;
+        const float v = part[i];
+        if (a.nsplit > 1) atomicAdd(a.acc + o, v);
+        else if (a.out_bf16) ((__nv_bfloat16 *)a.y)[o] = __float2bfloat16_rn(v);
+        else ((float *)a.y)[o] = v;
+    }
+}
+
+template <int NB, int LW, int FMT>
+cudaError_t launch_one(const TmaArgs &a, dim3 grid, int threads, size_t smem, cudaStream_t st)
+{
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<NB, LW, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<NB, LW, FMT>, a);
+}
+
+template <int NB, int LW>
+cudaError_t launch_lw(int fmt, const TmaArgs &a, dim3 grid, int threads, size_t smem, cudaStream_t st)
+{
+    if (fmt == FMT_PAL) return launch_one<NB, LW, FMT_PAL>(a, grid, threads, smem, st);
+    if (fmt == FMT_EXP) return launch_one<NB, LW, FMT_EXP>(a, grid, threads, smem, st);
+    return launch_one<NB, LW, FMT_BF16>(a, grid, threads, smem, st);
+}
+
+struct TmaShape {
+    int nsplit, ks, lw, wk, rs, stages, stage_bytes, rows_cta, bm_words, vcap, ctas;
+    size_t smem;
+};
+
+// Pick K-slice, lane width, rows per stage and ring depth for (N, K, B, fmt).
+//   max_warps : consumer warps per CTA (8 keeps a CTA at <= 288 threads, so two fit on an SM)
+//   per_sm    : CTAs per SM of this launch (1 leaves room for the next launch's CTA)
+// X lives in <= 64 bf16x2 registers per lane; shared memory per CTA stays under the per_sm share
+// (half of 227 KB when a second CTA - of this launch or of the next one - should fit beside it).
+bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int per_sm, size_t smem_cap, TmaShape &s)
+{
+    const int nb = B <= 1 ? 1 : 2;
+    const int max_x_regs = 64;  // bf16x2 registers: LW/2 per batch row
+    int split = std::max(1, split_k);
+    for (;; split++) {
+        if (split > 64) return false;
+        const int ks = (int)(((w.K + split - 1) / split + 63) / 64 * 64);
+        int lw = 32;
+        while (lw < 128 && (ks + 32 * lw - 1) / (32 * lw) > max_warps) lw *= 2;
+        const int wk = (ks + 32 * lw - 1) / (32 * lw);
+        if (wk > max_warps || lw / 2 * nb > max_x_regs) continue;
+        s.nsplit = (int)((w.K + ks - 1) / ks);
+        s.ks = ks;
+        s.lw = lw;
+        s.wk = wk;
+        break;
+    }
+    s.rs = std::max(1, std::min(4, max_warps / s.wk));
+    const int num = w.fmt == FMT_PAL ? 3 : 4, den = 2;
+    s.stage_bytes = (int)(((int64_t)s.rs * s.ks * num / den + 127) / 128 * 128);
+    const int groups = (int)((B + nb - 1) / nb);
+    s.ctas = std::max(1, num_sms() * per_sm / std::max(1, s.nsplit * groups));
+    s.ctas = (int)std::min<int64_t>(s.ctas, (w.N + s.rs - 1) / s.rs);
+    s.rows_cta = (int)((w.N + s.ctas - 1) / s.ctas) + 1;
+    s.bm_words = (int)((int64_t)s.rows_cta * (w.K / 64) / 32 + 2);
+    // staged verbatim blocks: up to ~3% of the CTA's blocks, at most 4 KB (the rest use global loads)
+    const int64_t cta_blocks = (int64_t)s.rows_cta * (w.K / 64);
+    s.vcap = w.fmt == FMT_PAL ? (int)std::min<int64_t>(64, std::max<int64_t>(16, cta_blocks * 3 / 100)) : 0;
+    const size_t fixed = kTableBytes + 1024 + ((size_t)s.rows_cta * nb * 4 + 1023) / 1024 * 1024 +
+                         2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024) + (size_t)s.vcap * 64;
+    if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
+    s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);
+    s.smem = fixed + (size_t)s.stages * s.stage_bytes;
+    return true;
+}
+
+struct Knobs {
+    int max_warps, per_sm;
+    size_t cap;
+};
+
+// variant 0: 8 consumer warps, 2 CTAs/SM; variant 2: 16 consumer warps, 1 CTA/SM with all shared memory;
+// variant 3: 8 consumer warps, 1 CTA/SM in half the shared memory (the next launch's CTA fits beside it).
+Knobs knobs_of(int variant)
+{
+    if (variant == 2) return Knobs{16, 1, 227 * 1024};
+    if (variant == 3) return Knobs{8, 1, 113 * 1024};
+    return Knobs{8, 2, 113 * 1024};
+}
+
+bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaShape &s)
+{
+    const Knobs k = knobs_of(variant);
+    return plan_shape(w, B, split_k, k.max_warps, k.per_sm, k.cap, s);
+}
+
+}  // namespace
+
+bool gemv_tma_supported(const WOperand &w, int64_t B, int variant)
+{
+    TmaShape s;
+    return variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 && plan_variant(w, B, 0, variant, s);
+}
+
+int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
+                    float *acc_ws, int *status, void *stream)
+{
+    TmaShape s;
+    if (!plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
+    const int nb = B <= 1 ? 1 : 2;
+    cudaStream_t st = (cudaStream_t)stream;
+    TmaArgs a{w, x, B, y, nullptr, out_bf16, s.nsplit, s.ks, s.rs, s.stages, s.wk, s.stage_bytes, s.rows_cta,
+              s.bm_words, s.vcap, w.w_from_prev, status};
+    if (s.nsplit > 1) {
+        a.acc = out_bf16 ? acc_ws : (float *)y;
+        if (!a.acc) return cudaErrorInvalidValue;
+        cudaError_t e = cudaMemsetAsync(a.acc, 0, (size_t)B * w.N * 4, st);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)s.ctas, (unsigned)s.nsplit, (unsigned)((B + nb - 1) / nb));
+    const int threads = 32 * (1 + s.rs * s.wk);
+    cudaError_t e;
+    if (nb == 1) {
+        e = s.lw == 32 ? launch_lw<1, 32>(w.fmt, a, grid, threads, s.smem, st)
+          : s.lw == 64 ? launch_lw<1, 64>(w.fmt, a, grid, threads, s.smem, st)
+                       : launch_lw<1, 128>(w.fmt, a, grid, threads, s.smem, st);
+    } else {
+        e = s.lw == 32 ? launch_lw<2, 32>(w.fmt, a, grid, threads, s.smem, st)
+                       : launch_lw<2, 64>(w.fmt, a, grid, threads, s.smem, st);
+    }
+    if (e != cudaSuccess) return e;
+    if (s.nsplit > 1 && out_bf16) return launch_finalize(acc_ws, y, B * w.N, 1, stream);
+    return cudaSuccess;
+}
+
+}  // namespace uw

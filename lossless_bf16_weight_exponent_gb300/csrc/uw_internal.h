@@ -75,6 +75,8 @@ struct WOperand {
     const uint8_t *verb_exp;  // FMT_PAL verbatim handling
     uint8_t palette[16];
     int64_t N, K;
+    int *status;              // device status word of the matrix
+    int w_from_prev;          // the weight stream was written by the preceding kernel (preprocess workspace)
 };
 
 // kernel launchers (k_decode.cu, k_gemv.cu, k_tc.cu); return cudaError_t as int
@@ -82,6 +84,11 @@ int launch_decode_palette(const DevView &v, int out_kind, void *out, void *strea
 int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream);
 int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k,
                 int variant, float *acc_ws, void *stream);
+// persistent bulk-copy GEMV (B <= 2); variant 0: 8 consumer warps, 2 CTAs/SM; 2: 16 warps, 1 CTA/SM with all
+// shared memory; 3: 8 warps, 1 CTA/SM in half the shared memory; 1: not this kernel (the plain-load GEMV)
+bool gemv_tma_supported(const WOperand &w, int64_t B, int variant);
+int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
+                    float *acc_ws, int *status, void *stream);
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);

@@ -256,6 +256,7 @@ static WOperand operand_shape(const uw_matrix *m, int strategy)
     w.prefix = m->v.prefix;
     w.verb_exp = m->v.verb_exp;
     w.codes = m->codes;
+    w.status = m->v.status;
     return w;
 }
 
@@ -362,15 +363,18 @@ extern "C" uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x, int64
         e = m->h.codec == UW_CODEC_PALETTE ? launch_decode_palette(m->v, DEC_BF16, wsp, stream)
                                            : launch_decode_huffman(m->v, DEC_BF16, wsp, stream);
         w.w = (const uint16_t *)wsp;
+        w.w_from_prev = 1;
         break;
     case UW_STRAT_EXP_ONLY:
         e = m->h.codec == UW_CODEC_PALETTE ? launch_decode_palette(m->v, DEC_EXP, wsp, stream)
                                            : launch_decode_huffman(m->v, DEC_EXP, wsp, stream);
         w.exps = wsp;
+        w.w_from_prev = 1;
         break;
     case UW_STRAT_PALETTE_TRANSCODE:
         e = launch_decode_huffman(m->v, DEC_CODES, wsp, stream);
         w.codes = wsp;
+        w.w_from_prev = 1;
         break;
     default: break;
     }
