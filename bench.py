@@ -42,7 +42,26 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-autotune", action="store_true")
     p.add_argument("--json-out", default=None)
+    p.add_argument("--workload", default="gate_8b",
+                   choices=["gate_8b", "down_8b", "gate_70b", "down_70b", "heavy_tail", "tiny"],
+                   help="matrix recipe (the JSON line's headline workload is gate_8b)")
+    p.add_argument("--plan", default=None, help="force a plan 'strategy,kernel,split,variant' (skips autotuning)")
     return p.parse_args()
+
+
+def workload_matrix(name):
+    import synth
+    if name == "gate_8b":
+        return synth.gate_8b()
+    if name == "down_8b":
+        return synth.stack_8b(1)[2]
+    if name == "gate_70b":
+        return synth.mlp_70b()[0]
+    if name == "down_70b":
+        return synth.mlp_70b()[2]
+    if name == "heavy_tail":
+        return synth.heavy_tail()
+    return synth.tiny()
 
 
 def peaks():
@@ -208,7 +227,7 @@ def run_ours(args):
     rank, world, local = dist_setup()
     dev = torch.cuda.current_device()
     B = args.batch
-    mat = synth.gate_8b()
+    mat = workload_matrix(args.workload)
     w = mat.weights()
     blob = uw.encode(w, uw.CODEC_HUFFMAN)
     base = uw.Matrix(blob, want_palette_form=True)
@@ -219,7 +238,12 @@ def run_ours(args):
 
     # autotune on one copy (batches of the workload), share the table with the others
     tune_batches = [1, 4, 16] if B in (1, 4, 16) else [B]
-    if not args.no_autotune:
+    if args.plan:
+        vals = [int(v) for v in args.plan.split(",")]
+        text = "%d %d %d %d %d 0\n" % (1 << max(0, (B - 1).bit_length()), *vals)
+        for m in mats:
+            m.tune_load(text)
+    elif not args.no_autotune:
         need = base.autotune_workspace_size(tune_batches)
         tws = torch.empty(need, dtype=torch.uint8, device="cuda")
         base.autotune(tune_batches, tws, need)
@@ -313,7 +337,7 @@ def run_ours(args):
     e2e_value = eff_bytes * world * e2e_steps / e2e_s / 1e9
 
     breakdown = {}
-    if not args.no_breakdown and rank == 0:
+    if not args.no_breakdown and rank == 0 and args.workload == "gate_8b":
         breakdown = strategy_breakdown(mats, mat, info, copies, hbm_peak)
 
     cpu = None
@@ -327,8 +351,8 @@ def run_ours(args):
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(W, 3),
             "ms_per_step": ms_step, "us_per_matmul": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: W[14336,4096] bf16 N(0,0.02) with 1e-4 of entries x100, "
-                                   f"Huffman blob + resident palette form; X[{B},4096] N(0,1)",
+            "config": {"workload": f"{args.workload}: W[{mat.N},{mat.K}] bf16 ({mat.name} recipe), "
+                                   f"Huffman blob + resident palette form; X[{B},{mat.K}] N(0,1)",
                        "batch": B, "plan": plan.as_tuple(), "copies_rotated": copies,
                        "l2": f"inputs larger than L2: {copies} copies x {resident / 1e6:.1f} MB resident",
                        "compression": {"huffman_bits_per_weight": 8 * info["blob_bytes"] / (mat.N * mat.K),

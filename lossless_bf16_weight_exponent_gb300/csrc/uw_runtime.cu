@@ -264,7 +264,7 @@ static int resolve_kernel(const uw_matrix *m, const uw_plan &p, int64_t B)
 {
     if (p.kernel != UW_KERNEL_AUTO) return p.kernel;
     WOperand w = operand_shape(m, p.strategy);
-    if (B > 8 && tc_supported(w, B, p.variant)) return UW_KERNEL_TC;
+    if (B > 2 && tc_supported(w, B, p.variant)) return UW_KERNEL_TC;
     return UW_KERNEL_GEMV;
 }
 
