@@ -13,6 +13,8 @@
 // its chunk's end offset, or hits an unassigned prefix, latches DEV_CORRUPT.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "uw_internal.h"
 
 namespace uw {
@@ -100,21 +102,73 @@ int launch_decode_palette(const DevView &v, int out_kind, void *out, void *strea
 }
 
 // ------------------------------------------------------------------------------ Huffman decode
-template <int OUT>
-__global__ void __launch_bounds__(128) decode_huffman_kernel(DevView v, void *out)
+constexpr int kDecThreads = 128;        // chunks per CTA
+constexpr int kBitWindowWords = 0;      // staged bit-stream words per CTA (0: read the stream from global memory)
+
+// 16 codes (a u64 of nibbles) -> 16 exponent bytes through the palette
+__device__ __forceinline__ uint4 exps_of_codes(uint64_t codes, const uint8_t *pal)
 {
-    extern __shared__ uint8_t dtab[];
-    __shared__ uint8_t pal[16];
-    const int L = (int)v.max_len;
-    {
-        const uint4 *src = (const uint4 *)v.dtab;
-        uint4 *dst = (uint4 *)dtab;
-        for (int i = threadIdx.x; i < (1 << L) / 16; i += blockDim.x) dst[i] = src[i];
-        if (threadIdx.x < 16) pal[threadIdx.x] = v.palette[threadIdx.x];
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint32_t c = (uint32_t)(codes >> (16 * q));
+        w[q] = (uint32_t)pal[c & 15] | ((uint32_t)pal[(c >> 4) & 15] << 8) | ((uint32_t)pal[(c >> 8) & 15] << 16) |
+               ((uint32_t)pal[(c >> 12) & 15] << 24);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 16 weights of bf16 from 16 sign+mantissa bytes and 16 exponent bytes, stored at o[0..1]
+__device__ __forceinline__ void store_bf16x16(uint4 *o, const uint4 &s, const uint4 &e)
+{
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) h[i] = bf16_of(byte_of(s, 2 * i), byte_of(e, 2 * i)) | (bf16_of(byte_of(s, 2 * i + 1), byte_of(e, 2 * i + 1)) << 16);
+    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// The non-verbatim blocks of a chunk are decoded as one stream of 64*m symbols (their codes are
+// concatenated in the bit string); each full word of 16 codes is routed to its block.  Chunks hold at most
+// kMaxChunkBlocks blocks on this path; larger chunks fall back to one stream per block of the same loop.
+constexpr int kMaxChunkBlocks = 8;
+
+template <int OUT>
+__global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, void *out)
+{
+    extern __shared__ uint32_t dsm[];
+    __shared__ uint16_t pal2[256];  // exponent pair of a code byte: pal[b & 15] | pal[b >> 4] << 8
+    const bool multi = v.mtab != nullptr;
+    const int L = multi ? 12 : (int)v.max_len;
+    const int tab_words = multi ? 4096 : max(4096, (1 << L) / 4);
+    uint32_t *mt = dsm;                               // multi-symbol table, or the single-symbol byte table
+    uint32_t *sbits = dsm + tab_words;                // [kBitWindowWords] this CTA's run of the bit stream
+    if (multi) {
+        const uint4 *src = (const uint4 *)v.mtab;
+        for (int i = threadIdx.x; i < 1024; i += blockDim.x) ((uint4 *)mt)[i] = src[i];
+    } else {
+        const uint4 *src = (const uint4 *)v.dtab;
+        for (int i = threadIdx.x; i < (1 << L) / 16; i += blockDim.x) ((uint4 *)mt)[i] = src[i];
+    }
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+        pal2[i] = (uint16_t)(v.palette[i & 15] | (v.palette[i >> 4] << 8));
+    const uint64_t c_first = (uint64_t)blockIdx.x * kDecThreads;
+    const uint64_t c_last = min((uint64_t)v.n_chunks, c_first + kDecThreads);
+    const uint32_t w_start = v.chunk_off[c_first] >> 5;
+    const uint32_t w_stop = ((v.chunk_off[c_last] + 31) >> 5) + 4;  // + lookahead words
+    const bool staged = kBitWindowWords > 0 && (w_stop - w_start) <= (uint32_t)kBitWindowWords;
+    if (staged)
+        for (uint32_t i = threadIdx.x; i < w_stop - w_start; i += blockDim.x) sbits[i] = v.bits[w_start + i];
     __syncthreads();
-    const uint64_t c = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
-    if (c >= v.n_chunks) return;
+    const uint8_t *dt = (const uint8_t *)mt;
+    const uint64_t c = c_first + threadIdx.x;
+    if (c >= c_last) return;
+    // next 32-bit word of the stream (absolute word number); a corrupt stream that runs past the staged window
+    // reads zeros there, and the chunk's length check below reports it
+    auto word_at = [&](uint32_t wn) -> uint32_t {
+        if (staged) return wn < w_stop ? sbits[wn - w_start] : 0u;
+        return v.bits[wn];
+    };
     const uint64_t n = (uint64_t)v.N * (uint64_t)v.K;
     const uint32_t pos0 = v.chunk_off[c], pos1 = v.chunk_off[c + 1];
     const uint64_t b0 = c * (v.chunk / 64);
@@ -122,69 +176,115 @@ __global__ void __launch_bounds__(128) decode_huffman_kernel(DevView v, void *ou
 
     uint32_t wi = pos0 >> 5;
     const int sh = pos0 & 31;
-    uint64_t buf = (((uint64_t)v.bits[wi] << 32) | v.bits[wi + 1]) << sh;
+    uint64_t buf = (((uint64_t)word_at(wi) << 32) | word_at(wi + 1)) << sh;
     int avail = 64 - sh;
     wi += 2;
     uint32_t used = 0;
     const uint32_t budget = pos1 - pos0;
     bool bad = false;
 
-    for (uint64_t b = b0; b < b1 && !bad; b++) {
-        const uint32_t bw = __ldg(v.bitmap + (b >> 5));
-        const bool verb = (bw >> (b & 31)) & 1u;
-        const uint8_t *ve = nullptr;
-        if (verb) ve = v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64;
-#pragma unroll 1
-        for (int q = 0; q < 4; q++) {  // 16 weights per step
-            uint32_t sym[16];
-            if (verb) {
-                if (OUT != DEC_CODES) {
-                    uint4 ev = *(const uint4 *)(ve + q * 16);
+    // emit 16 codes (one u64 word) of non-verbatim block b, quarter q
+    auto emit = [&](uint64_t b, int q, uint64_t cw) {
+        if (OUT == DEC_CODES) {
+            *(uint64_t *)((uint8_t *)out + b * 32 + q * 8) = cw;
+        } else {
+            uint32_t e[4];
 #pragma unroll
-                    for (int i = 0; i < 16; i++) sym[i] = byte_of(ev, i);
+            for (int i = 0; i < 4; i++) {
+                const uint32_t cb = (uint32_t)(cw >> (16 * i));
+                e[i] = (uint32_t)pal2[cb & 0xFF] | ((uint32_t)pal2[cb >> 8 & 0xFF] << 16);
+            }
+            const uint4 ev = make_uint4(e[0], e[1], e[2], e[3]);
+            if (OUT == DEC_EXP) {
+                *(uint4 *)((uint8_t *)out + b * 64 + q * 16) = ev;
+            } else {
+                const uint4 sv = *(const uint4 *)(v.sm + b * 64 + q * 16);
+                store_bf16x16((uint4 *)((uint16_t *)out + b * 64 + q * 16), sv, ev);
+            }
+        }
+    };
+
+    for (uint64_t bs = b0; bs < b1 && !bad; bs += kMaxChunkBlocks) {
+        const uint64_t be = min(b1, bs + kMaxChunkBlocks);
+        // bit j of nvmask: block bs + j is not verbatim; verbatim blocks are written here directly
+        uint32_t nvmask = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxChunkBlocks; j++) {
+            const uint64_t b = bs + j;
+            if (b >= be) break;
+            const uint32_t bw = __ldg(v.bitmap + (b >> 5));
+            if ((bw >> (b & 31)) & 1u) {
+                const uint4 *ve = (const uint4 *)(v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64);
+                if (OUT == DEC_CODES) {
+                    uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
+                    o[0] = make_uint4(0, 0, 0, 0);
+                    o[1] = make_uint4(0, 0, 0, 0);
+                } else if (OUT == DEC_EXP) {
+                    uint4 *o = (uint4 *)((uint8_t *)out + b * 64);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) o[q] = ve[q];
                 } else {
+                    uint4 *o = (uint4 *)((uint16_t *)out + b * 64);
+                    const uint4 *sp = (const uint4 *)(v.sm + b * 64);
 #pragma unroll
-                    for (int i = 0; i < 16; i++) sym[i] = 0;
+                    for (int q = 0; q < 4; q++) store_bf16x16(o + 2 * q, sp[q], ve[q]);
                 }
             } else {
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    if (avail < 32) {
-                        buf |= (uint64_t)v.bits[wi++] << (32 - avail);
-                        avail += 32;
-                    }
-                    uint32_t ent = dtab[(uint32_t)(buf >> (64 - L))];
-                    uint32_t len = ent & 15u;
-                    bad |= (len == 0);
-                    len = len ? len : 1;
-                    buf <<= len;
-                    avail -= (int)len;
-                    used += len;
-                    sym[i] = OUT == DEC_CODES ? (ent >> 4) : pal[ent >> 4];
+                nvmask |= 1u << j;
+            }
+        }
+        const int total = 64 * __popc(nvmask);
+        int produced = 0, fill = 0, word = 0;
+        uint64_t acc = 0;
+        auto put = [&](uint64_t bits4, int cnt) {  // bits4 holds exactly cnt codes
+            acc |= bits4 << (4 * fill);
+            fill += cnt;
+            if (fill >= 16) {
+                const uint64_t b = bs + __fns(nvmask, 0, (word >> 2) + 1);  // the (word/4)-th non-verbatim block
+                emit(b, word & 3, acc);
+                word++;
+                fill -= 16;
+                acc = fill ? bits4 >> (4 * (cnt - fill)) : 0;
+            }
+        };
+        if (multi) {
+            while (produced + 5 <= total) {
+                const uint32_t e = mt[(uint32_t)(buf >> 52)];
+                uint32_t len = e & 15u;
+                int cnt = (int)((e >> 4) & 7u);
+                if (len == 0) { bad = true; len = 1; cnt = 1; }
+                buf <<= len;
+                avail -= (int)len;
+                used += len;
+                if (avail < 32) {
+                    buf |= (uint64_t)word_at(wi++) << (32 - avail);
+                    avail += 32;
                 }
+                put(e >> 11, cnt);
+                produced += cnt;
             }
-            const uint64_t off = b * 64 + q * 16;
-            if (OUT == DEC_BF16) {
-                uint4 s = *(const uint4 *)(v.sm + off);
-                uint32_t h[8];
-#pragma unroll
-                for (int i = 0; i < 8; i++)
-                    h[i] = bf16_of(byte_of(s, 2 * i), sym[2 * i]) | (bf16_of(byte_of(s, 2 * i + 1), sym[2 * i + 1]) << 16);
-                uint4 *o = (uint4 *)((uint16_t *)out + off);
-                o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                o[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            } else if (OUT == DEC_EXP) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++)
-                    w4[i] = sym[4 * i] | (sym[4 * i + 1] << 8) | (sym[4 * i + 2] << 16) | (sym[4 * i + 3] << 24);
-                *(uint4 *)((uint8_t *)out + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        while (produced < total) {
+            uint32_t len, sym;
+            if (multi) {
+                const uint32_t e = mt[(uint32_t)(buf >> 52)];
+                len = (e >> 7) & 15u;
+                sym = (e >> 11) & 15u;
             } else {
-                uint32_t w2[2] = {0, 0};
-#pragma unroll
-                for (int i = 0; i < 16; i++) w2[i >> 3] |= sym[i] << (4 * (i & 7));
-                *(uint2 *)((uint8_t *)out + off / 2) = make_uint2(w2[0], w2[1]);
+                const uint32_t e = dt[(uint32_t)(buf >> (64 - L))];
+                len = e & 15u;
+                sym = e >> 4;
             }
+            if (len == 0) { bad = true; len = 1; }
+            buf <<= len;
+            avail -= (int)len;
+            used += len;
+            if (avail < 32) {
+                buf |= (uint64_t)word_at(wi++) << (32 - avail);
+                avail += 32;
+            }
+            put(sym, 1);
+            produced++;
         }
         if (used > budget) bad = true;  // overran the chunk: stop before reading further
     }
@@ -194,17 +294,18 @@ __global__ void __launch_bounds__(128) decode_huffman_kernel(DevView v, void *ou
 int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream)
 {
     if (!v.n_chunks) return cudaSuccess;
-    const int threads = 128;
+    const int threads = kDecThreads;
     const int blocks = (int)((v.n_chunks + threads - 1) / threads);
-    const size_t smem = (size_t)1 << v.max_len;
+    const size_t tab_bytes = v.mtab ? 16384 : std::max<size_t>(16384, (size_t)1 << v.max_len);
+    const size_t smem = tab_bytes + (size_t)kBitWindowWords * 4;  // decode table + bit window
     cudaStream_t st = (cudaStream_t)stream;
     static bool attr_set = false;  // set once, outside any stream capture (uw_load runs these kernels first)
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768);
+        cudaError_t e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_EXP>, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768);
+            e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_EXP>, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_CODES>, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768);
+            e = cudaFuncSetAttribute(decode_huffman_kernel<DEC_CODES>, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }

@@ -135,6 +135,33 @@ void build_decode_table(const uint8_t *lens, int max_len, std::vector<uint8_t> &
     }
 }
 
+// Multi-symbol decode table for limits <= 12: entry v (the next 12 bits of the stream) packs
+//   bits 0-3   total length of the whole codes it holds (<= 12)
+//   bits 4-6   how many whole codes start in v (1..5)
+//   bits 7-10  length of the first code
+//   bits 11-30 the codes' symbols, 4 bits each, first symbol lowest
+// 0 where no code matches v's prefix.
+void build_multi_table(const uint8_t *lens, std::vector<uint32_t> &table)
+{
+    std::vector<uint8_t> single;
+    build_decode_table(lens, 12, single);  // (symbol << 4) | length over 12-bit prefixes
+    table.assign(4096, 0);
+    for (uint32_t v = 0; v < 4096; v++) {
+        uint32_t used = 0, n = 0, first = 0, syms = 0;
+        while (n < 5) {
+            const uint32_t peek = (v << used) & 0xFFFu;  // next 12 bits, zero-filled past v's end
+            const uint8_t e = single[peek];
+            const uint32_t len = e & 15u;
+            if (!len || used + len > 12) break;
+            if (n == 0) first = len;
+            syms |= (uint32_t)(e >> 4) << (4 * n);
+            used += len;
+            n++;
+        }
+        if (n) table[v] = used | (n << 4) | (first << 7) | (syms << 11);
+    }
+}
+
 // ------------------------------------------------------------------------------ layout
 static void layout(const BlobHeader &h, uint64_t *off, uint64_t *len, uint64_t *total)
 {

@@ -36,6 +36,8 @@ void canonical_codes(const uint8_t *lens, uint32_t *codes);
 // Decode table for a canonical code: entry[v] for every max_len-bit prefix v is
 // (symbol << 4) | length, 0 where no code matches.
 void build_decode_table(const uint8_t *lens, int max_len, std::vector<uint8_t> &table);
+// Multi-symbol table over 12-bit windows (limits <= 12), see uw_host.cpp for the entry layout.
+void build_multi_table(const uint8_t *lens, std::vector<uint32_t> &table);
 
 // --------------------------------------------------------------------------------------------
 // Device view of a loaded matrix (plain pointers, passed by value to kernels).
@@ -53,6 +55,7 @@ struct DevView {
     const uint32_t *chunk_off;// [n_chunks+1] bit offsets (Huffman)
     const uint32_t *bits;     // Huffman bit string, MSB-first u32 words, + guard words
     const uint8_t *dtab;      // [1 << max_len] decode table (Huffman)
+    const uint32_t *mtab;     // [4096] multi-symbol decode table (Huffman, max_len <= 12), else nullptr
     int *status;              // device status word (0 = ok)
 };
 

@@ -105,6 +105,8 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     const uint64_t o_bits = take(h.len[S_BITS] + 512);
     const uint64_t tab_bytes = h.codec == UW_CODEC_HUFFMAN ? ((uint64_t)1 << h.max_len) : 16;
     const uint64_t o_tab = take(tab_bytes);
+    const bool multi = h.codec == UW_CODEC_HUFFMAN && h.max_len <= 12;
+    const uint64_t o_mtab = multi ? take(4096 * 4) : 0;
     const uint64_t o_st = take(256);
 
     uw_matrix *m = new (std::nothrow) uw_matrix();
@@ -127,10 +129,16 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
         (e = up(o_bits, S_BITS)))
         return fail_free(cuda_fail(e, "uw_load: upload"));
     std::vector<uint8_t> table;
+    std::vector<uint32_t> mtable;
     if (h.codec == UW_CODEC_HUFFMAN) {
         build_decode_table(h.code_len, (int)h.max_len, table);
         if ((e = cudaMemcpyAsync(d + o_tab, table.data(), table.size(), cudaMemcpyHostToDevice, st)))
             return fail_free(cuda_fail(e, "uw_load: table upload"));
+        if (multi) {
+            build_multi_table(h.code_len, mtable);
+            if ((e = cudaMemcpyAsync(d + o_mtab, mtable.data(), mtable.size() * 4, cudaMemcpyHostToDevice, st)))
+                return fail_free(cuda_fail(e, "uw_load: table upload"));
+        }
     }
     DevView &v = m->v;
     memset(&v, 0, sizeof v);
@@ -146,6 +154,7 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     v.chunk_off = (const uint32_t *)(d + o_co);
     v.bits = (const uint32_t *)(d + o_bits);
     v.dtab = d + o_tab;
+    v.mtab = multi ? (const uint32_t *)(d + o_mtab) : nullptr;
     v.status = (int *)(d + o_st);
     if (h.codec == UW_CODEC_HUFFMAN && want_palette_form) {
         if ((e = (cudaError_t)launch_decode_huffman(v, DEC_CODES, m->codes, st)))
