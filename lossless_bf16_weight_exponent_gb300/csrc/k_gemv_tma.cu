@@ -300,6 +300,22 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
             float acc0[NB], acc1[NB];
 #pragma unroll
             for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
+            // verbatim flags of the lane's groups this stage: bit 8g of `vwin` (groups are 8 blocks apart)
+            uint64_t vwin = 0;
+            uint32_t bl0 = 0;
+            if (FMT == FMT_PAL) {
+                bl0 = (uint32_t)(blk_lane0 + i * blk_stage);
+                if (G <= 4) {
+                    const uint64_t w2 = ((uint64_t)bm[(bl0 >> 5) + 1] << 32) | bm[bl0 >> 5];
+                    vwin = (w2 >> (bl0 & 31)) & (G == 1 ? 0x1ull : G == 2 ? 0x101ull : 0x01010101ull);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; g++) {
+                        const uint32_t bl = bl0 + 8 * g;
+                        vwin |= (uint64_t)((bm[bl >> 5] >> (bl & 31)) & 1u) << (8 * g);
+                    }
+                }
+            }
 #pragma unroll
             for (int g = 0; g < G; g++) {
                 const int kk = kbase + 512 * g;
@@ -308,9 +324,9 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
                     if (FMT == FMT_PAL) {
                         const uint4 s = *(const uint4 *)(st + slot_row * klen + kk);
                         const uint2 cc = *(const uint2 *)(st + a.rs * klen + slot_row * (klen / 2) + kk / 2);
-                        const uint32_t bl = (uint32_t)(blk_lane0 + i * blk_stage) + (uint32_t)(8 * g);  // 512 weights = 8 blocks
-                        const uint32_t bw = bm[bl >> 5];
-                        if (__builtin_expect((bw >> (bl & 31)) & 1u, 0)) {
+                        if (__builtin_expect(vwin != 0, 0) && ((vwin >> (8 * g)) & 1u)) {
+                            const uint32_t bl = bl0 + 8 * g;
+                            const uint32_t bw = bm[bl >> 5];
                             const uint64_t vi = pf[bl >> 5] + __popc(bw & ((1u << (bl & 31)) - 1u));
                             const uint64_t vl = vi - v_begin;
                             const int within = kk & 63;
@@ -416,7 +432,8 @@ struct TmaShape {
 //   per_sm    : CTAs per SM of this launch (1 leaves room for the next launch's CTA)
 // X lives in <= 64 bf16x2 registers per lane; shared memory per CTA stays under the per_sm share
 // (half of 227 KB when a second CTA - of this launch or of the next one - should fit beside it).
-bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int per_sm, size_t smem_cap, TmaShape &s)
+bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int per_sm, size_t smem_cap, int lw_pref,
+                TmaShape &s)
 {
     const int nb = B <= 1 ? 1 : 2;
     const int max_x_regs = 64;  // bf16x2 registers: LW/2 per batch row
@@ -424,7 +441,7 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     for (;; split++) {
         if (split > 64) return false;
         const int ks = (int)(((w.K + split - 1) / split + 63) / 64 * 64);
-        int lw = 32;
+        int lw = lw_pref;
         while (lw < 128 && (ks + 32 * lw - 1) / (32 * lw) > max_warps) lw *= 2;
         const int wk = (ks + 32 * lw - 1) / (32 * lw);
         if (wk > max_warps || lw / 2 * nb > max_x_regs) continue;
@@ -456,21 +473,28 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
 struct Knobs {
     int max_warps, per_sm;
     size_t cap;
+    int lw;
 };
 
-// variant 0: 8 consumer warps, 2 CTAs/SM; variant 2: 16 consumer warps, 1 CTA/SM with all shared memory;
-// variant 3: 8 consumer warps, 1 CTA/SM in half the shared memory (the next launch's CTA fits beside it).
+// Variants (1 is the plain-load GEMV, not this kernel):
+//   0: 8 consumer warps, 2 CTAs/SM, 32 weights per lane and row     4: as 0 with 64 weights per lane
+//   2: 16 consumer warps, 1 CTA/SM with all shared memory            5: as 2 with 64 weights per lane
+//   3: 8 consumer warps, 1 CTA/SM in half the shared memory (room for the next launch's CTA)
 Knobs knobs_of(int variant)
 {
-    if (variant == 2) return Knobs{16, 1, 227 * 1024};
-    if (variant == 3) return Knobs{8, 1, 113 * 1024};
-    return Knobs{8, 2, 113 * 1024};
+    switch (variant) {
+    case 2: return Knobs{16, 1, 227 * 1024, 32};
+    case 3: return Knobs{8, 1, 113 * 1024, 32};
+    case 4: return Knobs{8, 2, 113 * 1024, 64};
+    case 5: return Knobs{16, 1, 227 * 1024, 64};
+    default: return Knobs{8, 2, 113 * 1024, 32};
+    }
 }
 
 bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaShape &s)
 {
     const Knobs k = knobs_of(variant);
-    return plan_shape(w, B, split_k, k.max_warps, k.per_sm, k.cap, s);
+    return plan_shape(w, B, split_k, k.max_warps, k.per_sm, k.cap, k.lw, s);
 }
 
 }  // namespace

@@ -525,7 +525,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
                 if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_DIRECT_PALETTE; v++) if (strategy_ok(m, v)) values.push_back(v); }
                 else if (coord == 1) values = {UW_KERNEL_GEMV, UW_KERNEL_TC};
                 else if (coord == 2) values = split_candidates(m);
-                else values = {0, 1, 2, 3};
+                else values = {0, 1, 2, 3, 4, 5};
                 for (int v : values) {
                     uw_plan p = best;
                     if (coord == 0) p.strategy = v;
