@@ -15,9 +15,14 @@
 // slot c / WK of a stage and the c % WK-th piece of the K-slice: lane l owns the
 // weights k = piece*32*LW + 16*l + 512*g (g < LW/16), so its X values stay in
 // registers for the whole kernel and its 16-byte shared loads are bank-conflict
-// free.  Row partial sums meet in shared memory (atomic adds) and are written
-// once at the end.  Every mbarrier wait is bounded by a global-timer limit; on
-// expiry the kernel latches DEV_TIMEOUT, drains the copies it issued and returns.
+// free.  A consumer copies its part of a stage into registers and releases the
+// slot before computing on it.  Two 4-bit codes (one code byte) select the
+// exponent fields of a bf16x2 pair from a 32 KB per-lane table in shared memory,
+// so a warp's lookups never share a bank.  Lane sums of four consecutive stages
+// are reduced together (a transposed butterfly), and row sums meet in shared
+// memory and are written once at the end.  Every
+// mbarrier wait is bounded by a global-timer limit; on expiry the kernel latches
+// DEV_TIMEOUT, drains the copies it issued and returns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -130,15 +135,23 @@ __device__ __forceinline__ void pairs_from_exps(uint32_t S, uint32_t E, uint32_t
     p23 = __byte_perm(lo, hi, 0x7362u);
 }
 
-// Palette pair table: for a code byte b (codes c0 = b & 15, c1 = b >> 4) the exponent fields of the bf16x2
-// pair, (pal[c1] << 23) | (pal[c0] << 7), stored for each lane at byte offset 256*b + 4*lane.  A warp's 32
-// lookups always hit 32 different banks, and the offset of byte j of a code word C is a single byte
-// permute, [0, 0, byte j of C, 4*lane] (bytes 128..255 of each entry row are unused).
-constexpr int kTableBytes = 256 * 256;
-
-__device__ __forceinline__ uint32_t pair_exp(const uint8_t *tab, uint32_t C, uint32_t lane4, int j)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    return *(const uint32_t *)(tab + __byte_perm(C, lane4, 0x5504u | (uint32_t)(j << 4)));
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Palette pair table: for a code byte b (codes c0 = b & 15, c1 = b >> 4) the exponent fields of the bf16x2
+// pair, (pal[c1] << 23) | (pal[c0] << 7), stored for each lane at byte offset 128*b + 4*lane, so a warp's 32
+// lookups always hit 32 different banks.  The offset of byte j of a code word C is one byte extract and one
+// integer multiply-add (which the scheduler may issue on the FMA pipe, leaving the ALU pipe to the rebuild).
+constexpr int kTableBytes = 256 * 128;
+
+__device__ __forceinline__ uint32_t pair_exp(const uint8_t *tab_lane, uint32_t C, int j)
+{
+    const uint32_t b = prmt(C, 0u, 0x4440u | (uint32_t)j);  // byte j of C
+    return *(const uint32_t *)(tab_lane + b * 128u);
 }
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -149,6 +162,22 @@ template <int FMT> struct Fmt;
 template <> struct Fmt<FMT_PAL> { static constexpr int num = 3, den = 2; };   // sm + 4-bit code
 template <> struct Fmt<FMT_EXP> { static constexpr int num = 2, den = 1; };   // sm + exponent byte
 template <> struct Fmt<FMT_BF16> { static constexpr int num = 2, den = 1; };  // bf16
+
+// Sum each of v0..v3 over the warp's 32 lanes (a transposed butterfly: 6 shuffles for the four sums).
+// Lane L ends with the sum of v[((L >> 3) & 2) | ((L >> 3) & 1)], i.e. lanes 0, 8, 16, 24 hold sums 0..3.
+__device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3, int lane)
+{
+    const bool u16 = lane & 16, u8 = lane & 8;
+    const float s0 = u16 ? v0 : v2, s1 = u16 ? v1 : v3;  // what the partner keeps
+    const float k0 = u16 ? v2 : v0, k1 = u16 ? v3 : v1;
+    const float b0 = k0 + __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    const float b1 = k1 + __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    float c = (u8 ? b1 : b0) + __shfl_xor_sync(0xFFFFFFFFu, u8 ? b0 : b1, 8);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+    return c;
+}
 
 template <int NB, int LW, int FMT>
 __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
@@ -167,33 +196,21 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
     const uint64_t wb0 = ((uint64_t)r0 * K / 64) >> 5;
     const int n_bw = nrows ? (int)((((uint64_t)r1 * K / 64 - 1) >> 5) - wb0 + 1) : 0;
 
-    uint8_t *tab = smem;                                              // pair table (FMT_PAL)
-    uint64_t *full = (uint64_t *)(smem + kTableBytes);               // [stages]
-    uint64_t *empty = full + a.stages;                                // [stages]
-    float *part = (float *)(smem + kTableBytes + 1024);               // [rows_cta][NB]
+    constexpr int TB = FMT == FMT_PAL ? kTableBytes : 0;
+    uint8_t *tab = smem;                                                      // [TB] pair table
+    uint64_t *full = (uint64_t *)(smem + TB);                                 // [stages]
+    uint64_t *empty = full + a.stages;                                        // [stages]
+    uint64_t *vfull = empty + a.stages;                                       // staged verbatim exponents landed
+    float *part = (float *)(smem + TB + 1024);                                // [rows_cta][NB]
     const int part_bytes = (a.rows_cta * NB * 4 + 1023) / 1024 * 1024;
     const int bm_bytes = (a.bm_words * 4 + 1023) / 1024 * 1024;
-    uint32_t *bm = (uint32_t *)(smem + kTableBytes + 1024 + part_bytes);              // [bm_words] bitmap
-    uint32_t *pf = (uint32_t *)(smem + kTableBytes + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
-    uint8_t *vx = smem + kTableBytes + 1024 + part_bytes + 2 * bm_bytes;              // [vcap][64] verbatim exps
+    uint32_t *bm = (uint32_t *)(smem + TB + 1024 + part_bytes);              // [bm_words] bitmap
+    uint32_t *pf = (uint32_t *)(smem + TB + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
+    uint8_t *vx = smem + TB + 1024 + part_bytes + 2 * bm_bytes;              // [vcap][64] verbatim exps
     uint8_t *ring = vx + (size_t)a.vcap * 64;
-    uint64_t *vfull = empty + a.stages;                                                // verbatim staging barrier
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = a.rs * a.wk;  // consumer warps
-    if (FMT == FMT_PAL) {
-        // consecutive threads fill consecutive 16-byte chunks: bank-conflict-free stores
-        for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
-            const int b = i >> 3, q = i & 7;
-            const uint32_t v = ((uint32_t)a.w.palette[b >> 4] << 23) | ((uint32_t)a.w.palette[b & 15] << 7);
-            *(uint4 *)(tab + 256 * b + 16 * q) = make_uint4(v, v, v, v);
-        }
-        for (int i = threadIdx.x; i < n_bw; i += blockDim.x) {
-            bm[i] = __ldg(a.w.bitmap + wb0 + i);
-            pf[i] = __ldg(a.w.prefix + wb0 + i);
-        }
-    }
-    for (int i = threadIdx.x; i < a.rows_cta * NB; i += blockDim.x) part[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; s++) {
             mbar_init(&full[s], 1);
@@ -203,19 +220,6 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // verbatim blocks of the CTA's rows form one contiguous run of the verbatim stream: [v_begin, v_end)
-    uint64_t v_begin = 0;
-    int v_staged = 0;
-    if (FMT == FMT_PAL && nrows) {
-        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
-        const uint32_t w0 = bm[0];
-        v_begin = pf[0] + __popc(w0 & ((1u << (fb & 31)) - 1u));
-        const uint64_t lw = lb >> 5;
-        uint64_t v_end;
-        if (lw - wb0 < (uint64_t)n_bw) v_end = pf[lw - wb0] + __popc(bm[lw - wb0] & ((1u << (lb & 31)) - 1u));
-        else v_end = pf[n_bw - 1] + __popc(bm[n_bw - 1]);
-        v_staged = (int)(v_end - v_begin < (uint64_t)a.vcap ? v_end - v_begin : (uint64_t)a.vcap);
-    }
     // a dependent launch may start its prologue and stream its own weights from here on
     grid_launch_dependents();
 
@@ -223,15 +227,35 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
-            if (FMT == FMT_PAL) {
-                mbar_arrive_expect_tx(vfull, (uint32_t)v_staged * 64);
-                if (v_staged) bulk_g2s(vx, a.w.verb_exp + v_begin * 64, (uint32_t)v_staged * 64, vfull);
+            // the CTA's verbatim blocks form one contiguous run of the verbatim stream: [v_begin, v_end)
+            uint32_t bw0 = 0, pw0 = 0, bw1 = 0, pw1 = 0;
+            const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
+            const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
+            if (FMT == FMT_PAL && nrows) {
+                bw0 = __ldg(a.w.bitmap + (fb >> 5));
+                pw0 = __ldg(a.w.prefix + (fb >> 5));
+                bw1 = __ldg(a.w.bitmap + lwd);
+                pw1 = __ldg(a.w.prefix + lwd);
             }
+            if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
             int issued = 0;
             bool ok = true;
+            bool verb_issued = FMT != FMT_PAL;
             for (int i = 0; i < n_stages && ok; i++) {
                 const int slot = i % a.stages;
+                if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
+                    // the ring is primed: stage the verbatim run (its loads have landed meanwhile)
+                    uint32_t v_staged = 0;
+                    uint64_t v_begin = 0;
+                    if (nrows) {
+                        v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
+                        const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
+                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+                    }
+                    mbar_arrive_expect_tx(vfull, v_staged * 64);
+                    if (v_staged) bulk_g2s(vx, a.w.verb_exp + v_begin * 64, v_staged * 64, vfull);
+                    verb_issued = true;
+                }
                 if (i >= a.stages && !mbar_wait(&empty[slot], ((i / a.stages) - 1) & 1)) { ok = false; break; }
                 const int64_t g0 = r0 + (int64_t)i * a.rs;
                 const int nr = (int)min((int64_t)a.rs, r1 - g0);
@@ -251,9 +275,15 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
                 }
                 issued = i + 1;
             }
+            if (!verb_issued) {  // no stages (or a timeout before priming): complete the phase anyway
+                mbar_arrive_expect_tx(vfull, 0);
+                verb_issued = true;
+            }
+            // consumers wait for the staged verbatim run only when they meet a verbatim block: make sure the
+            // copy has landed before the CTA can exit
+            if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
             if (!ok) {
                 atomicExch(a.status, (int)DEV_TIMEOUT);
-                if (FMT == FMT_PAL) mbar_wait(vfull, 0);
                 // drain: every issued stage's copies must land before the CTA may exit
                 for (int i = max(0, issued - a.stages); i < issued; i++) mbar_wait(&full[i % a.stages], (i / a.stages) & 1);
             }
@@ -262,10 +292,26 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
     }
 
     // ---------------------------------------------------------------- consumers
+    const int ctid = threadIdx.x - 32;
+    if (FMT == FMT_PAL)
+        for (int i = ctid; i < a.bm_words; i += C * 32) {  // words past the CTA's blocks read as "not verbatim"
+            bm[i] = i < n_bw ? __ldg(a.w.bitmap + wb0 + i) : 0u;
+            pf[i] = i < n_bw ? __ldg(a.w.prefix + wb0 + i) : 0u;
+        }
+    for (int i = ctid; i < a.rows_cta * NB; i += C * 32) part[i] = 0.f;
     const int c = warp - 1;
     const int slot_row = c / a.wk, piece = c % a.wk;
     const int kbase = piece * 32 * LW + 16 * lane;
-    const uint32_t lane4 = 4u * (uint32_t)lane;
+    if (FMT == FMT_PAL) {
+        // entry row b holds the pair for code byte b once per lane: consecutive threads store consecutive
+        // 16-byte chunks (bank-conflict free)
+        for (int i = ctid; i < 256 * 8; i += C * 32) {
+            const int b = i >> 3, q = i & 7;
+            const uint32_t v = ((uint32_t)a.w.palette[b >> 4] << 23) | ((uint32_t)a.w.palette[b & 15] << 7);
+            *(uint4 *)(tab + 128 * b + 16 * q) = make_uint4(v, v, v, v);
+        }
+    }
+    const uint8_t *tab_lane = tab + 4 * lane;
     grid_dependency_wait();   // X (and Y, written below) belong to the stream order after the preceding kernel
     uint32_t xr[NB][LW / 2];  // bf16x2 activations of the lane's weights
 #pragma unroll
@@ -285,102 +331,159 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
                 xr[j][8 * g + 4 + q] = word_of(hi, q);
             }
         }
+    asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // bitmap words and zeroed row sums are in place
     // block index of the lane's first group in the first stage, relative to the CTA's first bitmap word
     const uint64_t blk_lane0 = (((uint64_t)(r0 + slot_row) * K + k0 + kbase) >> 6) - wb0 * 32;
     const uint64_t blk_stage = (uint64_t)a.rs * K / 64;
-    bool ok = true;
-    if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
+    bool ok = true, vx_ready = false;
+    uint64_t v_begin = 0;
+    uint32_t v_staged = 0;
+    float vs[4][NB];  // lane sums of the last four stages, oldest first, awaiting one joint reduction
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+#pragma unroll
+        for (int j = 0; j < NB; j++) vs[q][j] = 0.f;
     for (int i = 0; i < n_stages && ok; i++) {
         const int slot = i % a.stages;
         if (!mbar_wait(&full[slot], (i / a.stages) & 1)) { ok = false; break; }
-        const int64_t g0 = r0 + (int64_t)i * a.rs;
-        const int64_t row = g0 + slot_row;
-        if (row < r1) {
-            const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
-            float acc0[NB], acc1[NB];
-#pragma unroll
-            for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
-            // verbatim flags of the lane's groups this stage: bit 8g of `vwin` (groups are 8 blocks apart)
-            uint64_t vwin = 0;
-            uint32_t bl0 = 0;
-            if (FMT == FMT_PAL) {
-                bl0 = (uint32_t)(blk_lane0 + i * blk_stage);
-                if (G <= 4) {
-                    const uint64_t w2 = ((uint64_t)bm[(bl0 >> 5) + 1] << 32) | bm[bl0 >> 5];
-                    vwin = (w2 >> (bl0 & 31)) & (G == 1 ? 0x1ull : G == 2 ? 0x101ull : 0x01010101ull);
+        const int64_t row = r0 + (int64_t)i * a.rs + slot_row;
+        const bool live = row < r1;
+        const uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+        // the lane's 16 weights of group g: FMT_PAL sm bytes and codes (x1.x/.y); FMT_EXP sm and exponents;
+        // bf16 the two halves
+        auto load_group = [&](int g, uint4 &x0, uint4 &x1) {
+            const int kk = kbase + 512 * g;
+            x0 = x1 = make_uint4(0, 0, 0, 0);
+            if (live && kk < klen) {
+                if (FMT == FMT_PAL) {
+                    x0 = *(const uint4 *)(st + slot_row * klen + kk);
+                    const uint2 cc = *(const uint2 *)(st + a.rs * klen + slot_row * (klen / 2) + kk / 2);
+                    x1.x = cc.x;
+                    x1.y = cc.y;
+                } else if (FMT == FMT_EXP) {
+                    x0 = *(const uint4 *)(st + slot_row * klen + kk);
+                    x1 = *(const uint4 *)(st + a.rs * klen + slot_row * klen + kk);
                 } else {
-#pragma unroll
-                    for (int g = 0; g < G; g++) {
-                        const uint32_t bl = bl0 + 8 * g;
-                        vwin |= (uint64_t)((bm[bl >> 5] >> (bl & 31)) & 1u) << (8 * g);
-                    }
+                    x0 = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk);
+                    x1 = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk + 16);
                 }
             }
+        };
+        // small parts are copied into registers at once and the slot goes back to the producer before the
+        // compute; larger ones are read group by group and the slot is released after the compute
+        constexpr bool kEarly = G * NB <= 4;
+        uint4 d0[G], d1[G];
+        if (kEarly) {
 #pragma unroll
-            for (int g = 0; g < G; g++) {
-                const int kk = kbase + 512 * g;
-                if (kk < klen) {
-                    uint32_t pw[8];  // 8 bf16x2 pairs of weights
-                    if (FMT == FMT_PAL) {
-                        const uint4 s = *(const uint4 *)(st + slot_row * klen + kk);
-                        const uint2 cc = *(const uint2 *)(st + a.rs * klen + slot_row * (klen / 2) + kk / 2);
-                        if (__builtin_expect(vwin != 0, 0) && ((vwin >> (8 * g)) & 1u)) {
-                            const uint32_t bl = bl0 + 8 * g;
-                            const uint32_t bw = bm[bl >> 5];
-                            const uint64_t vi = pf[bl >> 5] + __popc(bw & ((1u << (bl & 31)) - 1u));
-                            const uint64_t vl = vi - v_begin;
-                            const int within = kk & 63;
-                            const uint4 ev = vl < (uint64_t)v_staged
-                                                 ? *(const uint4 *)(vx + vl * 64 + within)
-                                                 : __ldg((const uint4 *)(a.w.verb_exp + vi * 64 + within));
+            for (int g = 0; g < G; g++) load_group(g, d0[g], d1[g]);
+        }
+        // verbatim flags of the lane's groups this stage: bit 8g of `vwin` (groups are 8 blocks apart)
+        uint64_t vwin = 0;
+        uint32_t bl0 = 0;
+        if (FMT == FMT_PAL && live) {
+            bl0 = (uint32_t)(blk_lane0 + i * blk_stage);
+            if (G <= 4) {
+                const uint64_t w2 = ((uint64_t)bm[(bl0 >> 5) + 1] << 32) | bm[bl0 >> 5];
+                vwin = (w2 >> (bl0 & 31)) & (G == 1 ? 0x1ull : G == 2 ? 0x101ull : 0x01010101ull);
+            } else {
 #pragma unroll
-                            for (int q = 0; q < 4; q++) pairs_from_exps(word_of(s, q), word_of(ev, q), pw[2 * q], pw[2 * q + 1]);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; q++) {
-                                const uint32_t S = word_of(s, q);
-                                const uint32_t Cw = q < 2 ? cc.x : cc.y;
-                                const int jb = 2 * (q & 1);
-                                pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab, Cw, lane4, jb);
-                                pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab, Cw, lane4, jb + 1);
-                            }
-                        }
-                    } else if (FMT == FMT_EXP) {
-                        const uint4 s = *(const uint4 *)(st + slot_row * klen + kk);
-                        const uint4 e = *(const uint4 *)(st + a.rs * klen + slot_row * klen + kk);
-#pragma unroll
-                        for (int q = 0; q < 4; q++) pairs_from_exps(word_of(s, q), word_of(e, q), pw[2 * q], pw[2 * q + 1]);
-                    } else {
-                        const uint4 lo = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk);
-                        const uint4 hi = *(const uint4 *)(st + slot_row * 2 * klen + 2 * kk + 16);
-#pragma unroll
-                        for (int q = 0; q < 4; q++) { pw[q] = word_of(lo, q); pw[4 + q] = word_of(hi, q); }
-                    }
-#pragma unroll
-                    for (int j = 0; j < NB; j++)
-#pragma unroll
-                        for (int t = 0; t < 8; t += 2) {
-                            acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
-                            acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
-                        }
+                for (int g = 0; g < G; g++) {
+                    const uint32_t bl = bl0 + 8 * g;
+                    vwin |= (uint64_t)((bm[bl >> 5] >> (bl & 31)) & 1u) << (8 * g);
                 }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; j++) {
-                float v = acc0[j] + acc1[j];
-#pragma unroll
-                for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                if (lane == 0) atomicAdd(&part[(row - r0) * NB + j], v);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (kEarly) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+
+        float acc0[NB], acc1[NB];
+#pragma unroll
+        for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            if (!live || kbase + 512 * g >= klen) continue;  // past the CTA's rows or the K-slice
+            if (!kEarly) load_group(g, d0[g], d1[g]);
+            uint32_t pw[8];  // 8 bf16x2 pairs of weights
+            if (FMT == FMT_PAL) {
+                if (__builtin_expect(vwin != 0, 0) && ((vwin >> (8 * g)) & 1u)) {
+                    if (!vx_ready) {  // first verbatim block of this warp: the staged run must have landed
+                        if (!mbar_wait(vfull, 0)) ok = false;
+                        const uint64_t fb = (uint64_t)r0 * K / 64;
+                        const uint32_t w0 = bm[0];
+                        v_begin = pf[0] + __popc(w0 & ((1u << (fb & 31)) - 1u));
+                        const uint64_t lb = (uint64_t)r1 * K / 64, lw = lb >> 5;
+                        const uint64_t v_end = lw - wb0 < (uint64_t)n_bw
+                                                   ? pf[lw - wb0] + __popc(bm[lw - wb0] & ((1u << (lb & 31)) - 1u))
+                                                   : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
+                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+                        vx_ready = true;
+                    }
+                    const uint32_t bl = bl0 + 8 * g;
+                    const uint32_t bw = bm[bl >> 5];
+                    const uint64_t vi = pf[bl >> 5] + __popc(bw & ((1u << (bl & 31)) - 1u));
+                    const uint64_t vl = vi - v_begin;
+                    const int within = (kbase + 512 * g) & 63;
+                    const uint4 ev = vl < (uint64_t)v_staged ? *(const uint4 *)(vx + vl * 64 + within)
+                                                              : __ldg((const uint4 *)(a.w.verb_exp + vi * 64 + within));
+#pragma unroll
+                    for (int q = 0; q < 4; q++) pairs_from_exps(word_of(d0[g], q), word_of(ev, q), pw[2 * q], pw[2 * q + 1]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint32_t S = word_of(d0[g], q);
+                        const uint32_t Cw = q < 2 ? d1[g].x : d1[g].y;
+                        const int jb = 2 * (q & 1);
+                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb);
+                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb + 1);
+                    }
+                }
+            } else if (FMT == FMT_EXP) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) pairs_from_exps(word_of(d0[g], q), word_of(d1[g], q), pw[2 * q], pw[2 * q + 1]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[g], q); pw[4 + q] = word_of(d1[g], q); }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; j++)
+#pragma unroll
+                for (int t = 0; t < 8; t += 2) {
+                    acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
+                    acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
+                }
+        }
+        if (!kEarly) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        // shift the lane sum in; every fourth stage (and after the last) reduce four stages at once
+#pragma unroll
+        for (int j = 0; j < NB; j++) {
+            vs[0][j] = vs[1][j];
+            vs[1][j] = vs[2][j];
+            vs[2][j] = vs[3][j];
+            vs[3][j] = acc0[j] + acc1[j];
+        }
+        if ((i & 3) == 3 || i + 1 == n_stages) {
+#pragma unroll
+            for (int j = 0; j < NB; j++) {
+                const float v = reduce4(vs[0][j], vs[1][j], vs[2][j], vs[3][j], lane);
+                const int q = ((lane >> 3) & 2) | ((lane >> 3) & 1);
+                const int si = i - 3 + q;  // stage whose row sum this lane holds
+                const int64_t rw = r0 + (int64_t)si * a.rs + slot_row;
+                // stages before i & ~3 were reduced earlier (their slots hold zeros)
+                if ((lane & 7) == 0 && si >= (i & ~3) && rw < r1) atomicAdd(&part[(rw - r0) * NB + j], v);
+#pragma unroll
+                for (int t = 0; t < 4; t++) vs[t][j] = 0.f;
+            }
+        }
     }
     if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
     asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");
     // write the CTA's rows
-    const int tid = threadIdx.x - 32;
-    for (int i = tid; i < nrows * NB; i += C * 32) {
+    for (int i = ctid; i < nrows * NB; i += C * 32) {
         const int rl = i / NB, j = i - rl * NB;
         if (b0 + j >= a.B) continue;
         const int64_t o = (b0 + j) * N + r0 + rl;
@@ -462,7 +565,7 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     // staged verbatim blocks: up to ~3% of the CTA's blocks, at most 4 KB (the rest use global loads)
     const int64_t cta_blocks = (int64_t)s.rows_cta * (w.K / 64);
     s.vcap = w.fmt == FMT_PAL ? (int)std::min<int64_t>(64, std::max<int64_t>(16, cta_blocks * 3 / 100)) : 0;
-    const size_t fixed = kTableBytes + 1024 + ((size_t)s.rows_cta * nb * 4 + 1023) / 1024 * 1024 +
+    const size_t fixed = (w.fmt == FMT_PAL ? kTableBytes : 0) + 1024 + ((size_t)s.rows_cta * nb * 4 + 1023) / 1024 * 1024 +
                          2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024) + (size_t)s.vcap * 64;
     if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
     s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);

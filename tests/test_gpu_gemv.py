@@ -1,0 +1,56 @@
+"""GPU parity of every GEMV launch shape against the oracle's fp64 contraction.
+
+The fused reconstruct + GEMV of the Cloudflare blog "Unweight" (section on the
+reconstructive matmul) runs in several launch shapes that the autotuner may pick:
+consumer warps per CTA, CTAs per SM, weights per lane (32, 64 or 128), split-K.
+Each is checked on matrices that exercise its corner cases: many verbatim
+blocks (more than a CTA stages in shared memory), ragged row counts, a very long
+K, and a palette holding exponents of 128 and above (|w| >= 2)."""
+import numpy as np
+import pytest
+
+import lossless_bf16_weight_exponent_gb300 as uw
+import oracle
+import synth
+from uwtest import run_matmul, strategies_for, tol_ok
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = (0, 1, 2, 3, 4, 5)
+
+
+def _case(N, K, scale, p1, f1, seed):
+    w = synth.fill((N, K), seed=seed, scale=scale, p1=p1, f1=f1)
+    return w
+
+
+@pytest.mark.parametrize("N,K,scale,p1,f1", [
+    (300, 1024, 0.02, 0.005, 300.0),    # ~27% verbatim blocks
+    (257, 2112, 8.0, 0.0, 1.0),         # palette entries >= 128 (exponents around 130)
+    (96, 28672, 0.015, 1e-4, 100.0),    # long K: 128 weights per lane for 8-warp CTAs
+])
+@pytest.mark.parametrize("B", [1, 2])
+def test_gemv_variants(N, K, scale, p1, f1, B):
+    w = _case(N, K, scale, p1, f1, seed=N * 31 + K)
+    x = synth.fill((B, K), seed=N + K + B)
+    yref, absum = oracle.matmul(w, x)
+    for codec in (uw.CODEC_PALETTE, uw.CODEC_HUFFMAN):
+        m = uw.Matrix(uw.encode(w, codec), want_palette_form=True)
+        for s in strategies_for(m):
+            for v in VARIANTS:
+                for split in (0, 2):
+                    plan = (s, uw.KERNEL_GEMV, split, v)
+                    try:
+                        y = run_matmul(m, x, plan)
+                    except uw.UwError as e:  # a launch shape that does not fit this matrix
+                        assert e.status == uw.ERR_UNSUPPORTED, (plan, e)
+                        continue
+                    ok, worst = tol_ok(y, yref, absum)
+                    assert ok, (codec, plan, worst)
+
+
+def test_palette_high_exponents_present():
+    # the second case above must really put exponents >= 128 in the palette
+    w = _case(257, 2112, 8.0, 0.0, 1.0, seed=257 * 31 + 2112)
+    _, pal = oracle.palette(w)
+    assert max(pal) >= 128 and min(pal) < 128
