@@ -83,7 +83,7 @@ typedef enum { UW_OUT_F32 = 0, UW_OUT_BF16 = 1 } uw_out_dtype;
 /* Matmul kernel families. */
 typedef enum {
     UW_KERNEL_AUTO = 0,
-    UW_KERNEL_GEMV = 1,      /* CUDA-core GEMV, fp32 FMA, batch groups of up to 8 rows of X */
+    UW_KERNEL_GEMV = 1,      /* matrix-vector kernels for small B (see uw_plan.variant) */
     UW_KERNEL_TC = 2         /* tcgen05 tensor-core GEMM, W rebuilt in shared memory, fp32 in TMEM */
 } uw_kernel;
 
@@ -98,7 +98,15 @@ typedef struct {
     int32_t strategy;        /* uw_strategy, never AUTO inside a stored plan */
     int32_t kernel;          /* uw_kernel */
     int32_t split_k;         /* K-splits (>= 1); 0 = kernel's default */
-    int32_t variant;         /* kernel-specific tile / pipeline-depth selector; 0 = default */
+    int32_t variant;         /* kernel-specific launch shape; 0 = default.  UW_KERNEL_GEMV:
+                              *   0, 2..5: bulk-copy GEMV, fp32 FMA on CUDA cores, B <= 2 (0: 8 consumer warps,
+                              *            2 CTAs/SM; 2: 16 warps, 1 CTA/SM; 3: 8 warps, 1 CTA/SM in half the
+                              *            shared memory; 4, 5: as 0, 2 with 64 weights per lane)
+                              *   1:       plain-load GEMV, any B (batch groups of up to 8)
+                              *   6, 7:    GEMV on the tensor pipe (mma.sync, fp32 accumulate), B <= 16,
+                              *            K a multiple of 256 (6: K-slices of 4096 weights up to B = 8;
+                              *            7: of 2048)
+                              * a shape that does not fit the matrix or B runs the nearest one that does */
 } uw_plan;
 
 typedef struct {

@@ -321,9 +321,13 @@ int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int ou
 {
     if (B <= 0 || w.N == 0) return cudaSuccess;
     cudaStream_t st = (cudaStream_t)stream;
+    if ((variant == 6 || variant == 7) && w.K > 0 && gemv_mma_supported(w, B, variant)) {
+        const int e = launch_gemv_mma(w, x, B, y, out_bf16, split_k, variant, acc_ws, w.status, stream);
+        if (e != cudaErrorInvalidValue) return e;  // else: no tensor map for these operands, use the CUDA-core GEMV
+    }
     if (variant != 1 && w.K > 0) {
         // the default (variant 0) falls back to the one-CTA-per-SM shape when two CTAs do not fit
-        const int v = (variant == 0 && !gemv_tma_supported(w, B, 0)) ? 2 : variant;
+        const int v = (variant == 0 || variant > 5) && !gemv_tma_supported(w, B, 0) ? 2 : variant > 5 ? 0 : variant;
         if (gemv_tma_supported(w, B, v)) return launch_gemv_tma(w, x, B, y, out_bf16, split_k, v, acc_ws, w.status, stream);
     }
     const int nb = batch_group(B);

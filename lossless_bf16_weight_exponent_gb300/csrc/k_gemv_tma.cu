@@ -23,10 +23,13 @@
 // memory and are written once at the end.  Every
 // mbarrier wait is bounded by a global-timer limit; on expiry the kernel latches
 // DEV_TIMEOUT, drains the copies it issued and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "uw_internal.h"
 
@@ -36,7 +39,12 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait: far above any legitimate stall
 
-struct TmaArgs {
+struct TmaArgs {  // 64-byte aligned through its tensor maps
+    // whole-stage tensor copies (tmap != 0): the weight streams seen as [rows][2048-weight chunks][chunk bytes]
+    // in 8-byte elements, one box = one stage (rs rows x the K-slice)
+    CUtensorMap tm0;  // sm bytes, or bf16 weights
+    CUtensorMap tm1;  // codes or exponent bytes
+    int tmap;
     WOperand w;
     const uint16_t *x;
     int64_t B;
@@ -111,6 +119,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -180,7 +197,7 @@ __device__ __forceinline__ float reduce4(float v0, float v1, float v2, float v3,
 }
 
 template <int NB, int LW, int FMT>
-__global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
+__global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant__ TmaArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int G = LW / 16;
@@ -207,11 +224,15 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
     uint32_t *bm = (uint32_t *)(smem + TB + 1024 + part_bytes);              // [bm_words] bitmap
     uint32_t *pf = (uint32_t *)(smem + TB + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
     uint8_t *vx = smem + TB + 1024 + part_bytes + 2 * bm_bytes;              // [vcap][64] verbatim exps
-    uint8_t *ring = vx + (size_t)a.vcap * 64;
+    uint8_t *ring = vx + ((size_t)a.vcap * 64 + 1023) / 1024 * 1024;  // 1024-aligned: tensor copies want 128
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = a.rs * a.wk;  // consumer warps
     if (threadIdx.x == 0) {
+        if (a.tmap) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tm0) : "memory");
+            if (FMT != FMT_BF16) asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tm1) : "memory");
+        }
         for (int s = 0; s < a.stages; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C);
@@ -226,59 +247,69 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(TmaArgs a)
     const uint32_t wbytes = (uint32_t)((int64_t)klen * Fmt<FMT>::num / Fmt<FMT>::den);  // per row
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            // the CTA's verbatim blocks form one contiguous run of the verbatim stream: [v_begin, v_end)
-            uint32_t bw0 = 0, pw0 = 0, bw1 = 0, pw1 = 0;
-            const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
-            const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
-            if (FMT == FMT_PAL && nrows) {
-                bw0 = __ldg(a.w.bitmap + (fb >> 5));
-                pw0 = __ldg(a.w.prefix + (fb >> 5));
-                bw1 = __ldg(a.w.bitmap + lwd);
-                pw1 = __ldg(a.w.prefix + lwd);
-            }
-            if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
-            int issued = 0;
-            bool ok = true;
-            bool verb_issued = FMT != FMT_PAL;
-            for (int i = 0; i < n_stages && ok; i++) {
-                const int slot = i % a.stages;
-                if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
-                    // the ring is primed: stage the verbatim run (its loads have landed meanwhile)
+        // lane 0 runs the ring's barriers; lane r issues the copies of row r of each stage, so a stage's copies
+        // leave in one warp instruction rather than one after another
+        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
+        if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
+        int issued = 0;
+        bool ok = true;
+        bool verb_issued = FMT != FMT_PAL;
+        for (int i = 0; i < n_stages; i++) {
+            const int slot = i % a.stages;
+            if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
+                // the ring is primed: stage the CTA's verbatim blocks, one contiguous run [v_begin, v_end) of the
+                // verbatim stream
+                if (lane == 0) {
                     uint32_t v_staged = 0;
                     uint64_t v_begin = 0;
                     if (nrows) {
+                        const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
+                        const uint32_t bw0 = __ldg(a.w.bitmap + (fb >> 5)), pw0 = __ldg(a.w.prefix + (fb >> 5));
+                        const uint32_t bw1 = __ldg(a.w.bitmap + lwd), pw1 = __ldg(a.w.prefix + lwd);
                         v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
                         const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
                         v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
                     }
                     mbar_arrive_expect_tx(vfull, v_staged * 64);
                     if (v_staged) bulk_g2s(vx, a.w.verb_exp + v_begin * 64, v_staged * 64, vfull);
-                    verb_issued = true;
                 }
-                if (i >= a.stages && !mbar_wait(&empty[slot], ((i / a.stages) - 1) & 1)) { ok = false; break; }
-                const int64_t g0 = r0 + (int64_t)i * a.rs;
-                const int nr = (int)min((int64_t)a.rs, r1 - g0);
-                uint8_t *st = ring + (size_t)slot * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[slot], wbytes * nr);
-                for (int r = 0; r < nr; r++) {
-                    const uint64_t off = (uint64_t)(g0 + r) * K + k0;
-                    if (FMT == FMT_PAL) {
-                        bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
-                        bulk_g2s(st + a.rs * klen + r * (klen / 2), a.w.codes + off / 2, klen / 2, &full[slot]);
-                    } else if (FMT == FMT_EXP) {
-                        bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
-                        bulk_g2s(st + a.rs * klen + r * klen, a.w.exps + off, klen, &full[slot]);
-                    } else {
-                        bulk_g2s(st + r * 2 * klen, a.w.w + off, 2 * klen, &full[slot]);
-                    }
-                }
-                issued = i + 1;
-            }
-            if (!verb_issued) {  // no stages (or a timeout before priming): complete the phase anyway
-                mbar_arrive_expect_tx(vfull, 0);
                 verb_issued = true;
             }
+            const int64_t g0 = r0 + (int64_t)i * a.rs;
+            const int nr = (int)min((int64_t)a.rs, r1 - g0);
+            const bool whole = a.tmap && nr == a.rs && klen == a.ks;  // one tensor copy per stream: the whole stage
+            uint8_t *st = ring + (size_t)slot * a.stage_bytes;
+            int go = 1;
+            if (lane == 0) {
+                if (i >= a.stages && !mbar_wait(&empty[slot], ((i / a.stages) - 1) & 1)) go = 0;
+                else {
+                    mbar_arrive_expect_tx(&full[slot], wbytes * nr);
+                    if (whole) {
+                        if (FMT == FMT_BF16) tma3d(st, &a.tm0, 0, (int)(k0 >> 10), (int)g0, &full[slot]);
+                        else {
+                            tma3d(st, &a.tm0, 0, (int)(k0 >> 11), (int)g0, &full[slot]);
+                            tma3d(st + a.rs * klen, &a.tm1, 0, (int)(k0 >> 11), (int)g0, &full[slot]);
+                        }
+                    }
+                }
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, go, 0)) { ok = false; break; }
+            for (int r = whole ? 32 : lane; r < nr; r += 32) {
+                const uint64_t off = (uint64_t)(g0 + r) * K + k0;
+                if (FMT == FMT_PAL) {
+                    bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
+                    bulk_g2s(st + a.rs * klen + r * (klen / 2), a.w.codes + off / 2, klen / 2, &full[slot]);
+                } else if (FMT == FMT_EXP) {
+                    bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
+                    bulk_g2s(st + a.rs * klen + r * klen, a.w.exps + off, klen, &full[slot]);
+                } else {
+                    bulk_g2s(st + r * 2 * klen, a.w.w + off, 2 * klen, &full[slot]);
+                }
+            }
+            issued = i + 1;
+        }
+        if (lane == 0) {
+            if (!verb_issued) mbar_arrive_expect_tx(vfull, 0);  // no stages (or a timeout before priming)
             // consumers wait for the staged verbatim run only when they meet a verbatim block: make sure the
             // copy has landed before the CTA can exit
             if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
@@ -543,7 +574,9 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     int split = std::max(1, split_k);
     for (;; split++) {
         if (split > 64) return false;
-        const int ks = (int)(((w.K + split - 1) / split + 63) / 64 * 64);
+        // K-slices of whole 2048-weight chunks when K allows, so stages can move as single tensor copies
+        const int gran = w.K % 2048 == 0 ? 2048 : 64;
+        const int ks = (int)(((w.K + split - 1) / split + gran - 1) / gran * gran);
         int lw = lw_pref;
         while (lw < 128 && (ks + 32 * lw - 1) / (32 * lw) > max_warps) lw *= 2;
         const int wk = (ks + 32 * lw - 1) / (32 * lw);
@@ -554,7 +587,7 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
         s.wk = wk;
         break;
     }
-    s.rs = std::max(1, std::min(4, max_warps / s.wk));
+    s.rs = std::max(1, std::min(8, max_warps / s.wk));
     const int num = w.fmt == FMT_PAL ? 3 : 4, den = 2;
     s.stage_bytes = (int)(((int64_t)s.rs * s.ks * num / den + 127) / 128 * 128);
     const int groups = (int)((B + nb - 1) / nb);
@@ -566,11 +599,41 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     const int64_t cta_blocks = (int64_t)s.rows_cta * (w.K / 64);
     s.vcap = w.fmt == FMT_PAL ? (int)std::min<int64_t>(64, std::max<int64_t>(16, cta_blocks * 3 / 100)) : 0;
     const size_t fixed = (w.fmt == FMT_PAL ? kTableBytes : 0) + 1024 + ((size_t)s.rows_cta * nb * 4 + 1023) / 1024 * 1024 +
-                         2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024) + (size_t)s.vcap * 64;
+                         2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024) + ((size_t)s.vcap * 64 + 1023) / 1024 * 1024;
     if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
     s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);
     s.smem = fixed + (size_t)s.stages * s.stage_bytes;
     return true;
+}
+
+// Tensor maps that move one whole stage (rs rows x one K-slice) per stream in a single copy.  A row of a
+// stream is split into chunks of 2048 weights (sm and exponent bytes: 2048 B; codes: 1024 B; bf16 weights:
+// 1024 weights = 2048 B per chunk), each chunk a run of 8-byte elements, so the box is {chunk, chunks per
+// slice, rs} and lands in shared memory row after row exactly like the per-row copies.  Needs K and the
+// slice to be whole chunks; otherwise the kernel falls back to per-row bulk copies.
+bool make_stage_maps(const WOperand &w, const TmaShape &s, CUtensorMap &m0, CUtensorMap &m1)
+{
+    auto enc = (PFN_cuTensorMapEncodeTiled_v12000)tensor_map_encoder();
+    if (!enc || w.K % 2048 || s.ks % 2048 || w.N <= 0) return false;
+    auto make = [&](CUtensorMap &m, const void *base, uint64_t chunk_bytes, uint64_t chunks, uint64_t row_bytes,
+                    uint32_t box_chunks) {
+        if (!base || ((uintptr_t)base & 15) || box_chunks > 256 || s.rs > 256) return false;
+        cuuint64_t dims[3] = {chunk_bytes / 8, chunks, (cuuint64_t)w.N};
+        cuuint64_t strides[2] = {chunk_bytes, row_bytes};
+        cuuint32_t box[3] = {(cuuint32_t)(chunk_bytes / 8), box_chunks, (cuuint32_t)s.rs};
+        cuuint32_t estr[3] = {1, 1, 1};
+        return enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    const uint64_t K = (uint64_t)w.K, ks = (uint64_t)s.ks;
+    if (w.fmt == FMT_PAL)
+        return make(m0, w.sm, 2048, K / 2048, K, (uint32_t)(ks / 2048)) &&
+               make(m1, w.codes, 1024, K / 2048, K / 2, (uint32_t)(ks / 2048));
+    if (w.fmt == FMT_EXP)
+        return make(m0, w.sm, 2048, K / 2048, K, (uint32_t)(ks / 2048)) &&
+               make(m1, w.exps, 2048, K / 2048, K, (uint32_t)(ks / 2048));
+    return make(m0, w.w, 2048, K / 1024, 2 * K, (uint32_t)(ks / 1024));
 }
 
 struct Knobs {
@@ -615,8 +678,26 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
     if (!plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
     const int nb = B <= 1 ? 1 : 2;
     cudaStream_t st = (cudaStream_t)stream;
-    TmaArgs a{w, x, B, y, nullptr, out_bf16, s.nsplit, s.ks, s.rs, s.stages, s.wk, s.stage_bytes, s.rows_cta,
-              s.bm_words, s.vcap, w.w_from_prev, status};
+    TmaArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.w = w;
+    a.x = x;
+    a.B = B;
+    a.y = y;
+    a.acc = nullptr;
+    a.out_bf16 = out_bf16;
+    a.nsplit = s.nsplit;
+    a.ks = s.ks;
+    a.rs = s.rs;
+    a.stages = s.stages;
+    a.wk = s.wk;
+    a.stage_bytes = s.stage_bytes;
+    a.rows_cta = s.rows_cta;
+    a.bm_words = s.bm_words;
+    a.vcap = s.vcap;
+    a.w_from_prev = w.w_from_prev;
+    a.status = status;
+    a.tmap = make_stage_maps(w, s, a.tm0, a.tm1) ? 1 : 0;
     if (s.nsplit > 1) {
         a.acc = out_bf16 ? acc_ws : (float *)y;
         if (!a.acc) return cudaErrorInvalidValue;

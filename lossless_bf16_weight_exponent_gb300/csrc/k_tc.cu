@@ -425,19 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
-    });
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return (PFN_cuTensorMapEncodeTiled_v12000)tensor_map_encoder(); }
 
 bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128)
@@ -582,6 +570,20 @@ int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_
     if (e != cudaSuccess) return e;
     if (s.nsplit > 1 && out_bf16) return launch_finalize(acc_ws, y, B * w.N, 1, stream);
     return cudaSuccess;
+}
+
+void *tensor_map_encoder()
+{
+    static void *fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    });
+    return fn;
 }
 
 }  // namespace uw

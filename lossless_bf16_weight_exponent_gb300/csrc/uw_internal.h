@@ -92,6 +92,11 @@ int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int ou
 bool gemv_tma_supported(const WOperand &w, int64_t B, int variant);
 int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
                     float *acc_ws, int *status, void *stream);
+// GEMV on the tensor pipe (mma.sync m16n8k16) for B <= 16, 16 consumer warps, 1 CTA/SM; variant 6: 256
+// weights of a K-slice per warp (128 when B > 8); 7: 128
+bool gemv_mma_supported(const WOperand &w, int64_t B, int variant);
+int launch_gemv_mma(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
+                    float *acc_ws, int *status, void *stream);
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);
@@ -99,5 +104,7 @@ bool tc_supported(const WOperand &w, int64_t B, int variant);
 int gemv_default_split(const WOperand &w, int64_t B);
 int tc_default_split(const WOperand &w, int64_t B, int variant);
 int num_sms();
+// cuTensorMapEncodeTiled from the driver (nullptr when the driver lacks it)
+void *tensor_map_encoder();
 
 }  // namespace uw

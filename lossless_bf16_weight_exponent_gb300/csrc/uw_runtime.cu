@@ -292,7 +292,15 @@ static uw_plan default_plan(const uw_matrix *m, int64_t B)
     uw_plan p{};
     p.strategy = m->codes ? UW_STRAT_DIRECT_PALETTE : UW_STRAT_PALETTE_TRANSCODE;
     p.kernel = UW_KERNEL_AUTO;
+    const WOperand w = operand_shape(m, p.strategy);
+    if (B > 2 && B <= 16 && gemv_mma_supported(w, B, 6)) {
+        // a few batch rows: the tensor-pipe GEMV streams the weights once for all of them
+        p.kernel = UW_KERNEL_GEMV;
+        p.variant = 6;
+        return p;
+    }
     p.kernel = resolve_kernel(m, p, B);
+    if (p.kernel == UW_KERNEL_GEMV && gemv_tma_supported(w, B, 4)) p.variant = 4;
     return p;
 }
 
@@ -517,6 +525,18 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
         if (best.kernel == UW_KERNEL_AUTO) best.kernel = resolve_kernel(m, best, B);
         float best_us = 0;
         if (!time_plan(best, &best_us)) best_us = 3.0e38f;
+        // seeds the coordinate descent could not reach one coordinate at a time: each GEMV launch shape and the
+        // tensor-core kernel, on the default strategy
+        {
+            std::vector<uw_plan> seeds;
+            for (int v = 0; v <= 7; v++) seeds.push_back(uw_plan{best.strategy, UW_KERNEL_GEMV, 0, v});
+            seeds.push_back(uw_plan{best.strategy, UW_KERNEL_TC, 0, 0});
+            for (const uw_plan &p : seeds) {
+                if (memcmp(&p, &best, sizeof p) == 0) continue;
+                float us;
+                if (time_plan(p, &us) && us < best_us * 0.98f) { best = p; best_us = us; }
+            }
+        }
         // coordinate descent over (strategy, kernel, split, variant)
         for (int round = 0; round < 3; round++) {
             bool improved = false;
@@ -525,7 +545,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
                 if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_DIRECT_PALETTE; v++) if (strategy_ok(m, v)) values.push_back(v); }
                 else if (coord == 1) values = {UW_KERNEL_GEMV, UW_KERNEL_TC};
                 else if (coord == 2) values = split_candidates(m);
-                else values = {0, 1, 2, 3, 4, 5};
+                else values = {0, 1, 2, 3, 4, 5, 6, 7};
                 for (int v : values) {
                     uw_plan p = best;
                     if (coord == 0) p.strategy = v;

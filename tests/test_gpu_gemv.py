@@ -2,7 +2,8 @@
 
 The fused reconstruct + GEMV of the Cloudflare blog "Unweight" (section on the
 reconstructive matmul) runs in several launch shapes that the autotuner may pick:
-consumer warps per CTA, CTAs per SM, weights per lane (32, 64 or 128), split-K.
+consumer warps per CTA, CTAs per SM, weights per lane (32, 64 or 128), split-K,
+and the tensor-pipe GEMV (mma.sync, batch up to 16).
 Each is checked on matrices that exercise its corner cases: many verbatim
 blocks (more than a CTA stages in shared memory), ragged row counts, a very long
 K, and a palette holding exponents of 128 and above (|w| >= 2)."""
@@ -16,7 +17,7 @@ from uwtest import run_matmul, strategies_for, tol_ok
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = (0, 1, 2, 3, 4, 5)
+VARIANTS = (0, 1, 2, 3, 4, 5, 6, 7)
 
 
 def _case(N, K, scale, p1, f1, seed):
@@ -29,7 +30,7 @@ def _case(N, K, scale, p1, f1, seed):
     (257, 2112, 8.0, 0.0, 1.0),         # palette entries >= 128 (exponents around 130)
     (96, 28672, 0.015, 1e-4, 100.0),    # long K: 128 weights per lane for 8-warp CTAs
 ])
-@pytest.mark.parametrize("B", [1, 2])
+@pytest.mark.parametrize("B", [1, 2, 5, 16])
 def test_gemv_variants(N, K, scale, p1, f1, B):
     w = _case(N, K, scale, p1, f1, seed=N * 31 + K)
     x = synth.fill((B, K), seed=N + K + B)
@@ -54,3 +55,20 @@ def test_palette_high_exponents_present():
     w = _case(257, 2112, 8.0, 0.0, 1.0, seed=257 * 31 + 2112)
     _, pal = oracle.palette(w)
     assert max(pal) >= 128 and min(pal) < 128
+
+
+@pytest.mark.parametrize("B", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
+def test_mma_gemv_gate_8b_sampled(B, out_dtype):
+    # the tensor-pipe GEMV at full size, in the launch shapes the autotuner chooses from, on sampled rows
+    mat = synth.gate_8b()
+    w = mat.weights()
+    x = mat.activations(B)
+    rng = np.random.default_rng(B)
+    rows = np.unique(np.concatenate([[0, 7, 8, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
+    yref, absum = oracle.matmul(w, x, rows)
+    m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
+    for v in (6, 7):
+        y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_GEMV, 0, v), out_dtype)[:, rows]
+        ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
+        assert ok, (v, worst)
