@@ -106,6 +106,8 @@ typedef struct {
                               *   6, 7:    GEMV on the tensor pipe (mma.sync, fp32 accumulate), B <= 16,
                               *            K a multiple of 256 (6: K-slices of 4096 weights up to B = 8;
                               *            7: of 2048)
+                              * UW_KERNEL_TC: 0, 1: rebuilt tiles in shared memory; 2: rebuilt weights in tensor
+                              *   memory (B <= 256)
                               * a shape that does not fit the matrix or B runs the nearest one that does */
 } uw_plan;
 

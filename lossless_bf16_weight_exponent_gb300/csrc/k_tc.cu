@@ -7,13 +7,13 @@
 // Blackwell form: tcgen05.mma with the fp32 accumulator in tensor memory.
 //
 // One CTA owns a tile of 128 rows of W (the MMA's M) and a range of K.  Per 64-wide K-stage:
-//   - warp 8 (one thread) TMA-loads the sign+mantissa tile [128 x 64] u8, the 4-bit code tile [128 x 32] u8
+//   - warp 16 (one thread) TMA-loads the sign+mantissa tile [128 x 64] u8, the 4-bit code tile [128 x 32] u8
 //     (or the exponent tile, or - full-decode pipeline - the bf16 tile straight into the MMA layout) and the
 //     X tile [BN x 64] bf16 with 128-byte swizzle; one mbarrier counts the bytes;
-//   - warps 0-7 rebuild BF16 from the staged bytes into the K-major SWIZZLE_128B layout tcgen05 reads (row r,
-//     16-byte chunk c at (r/8)*1024 + (r%8)*128 + ((c ^ (r%8)) * 16)), fence the generic-proxy writes for the
-//     async proxy and arrive on a second mbarrier;
-//   - one thread of warp 9 issues four tcgen05.mma (M=128, N=BN <= 256, K=16; a second MMA for columns
+//   - warps 0-15 (two groups of eight taking alternate K-stages) rebuild BF16 from the staged bytes into the
+//     K-major SWIZZLE_128B layout tcgen05 reads (row r, 16-byte chunk c at (r/8)*1024 + (r%8)*128 +
+//     ((c ^ (r%8)) * 16)), fence the generic-proxy writes for the async proxy and arrive on a second mbarrier;
+//   - one thread of warp 17 issues four tcgen05.mma (M=128, N=BN <= 256, K=16; a second MMA for columns
 //     256..511) accumulating in TMEM, and tcgen05.commit releases the stage when they complete.
 // Epilogue: warps 0-3 read their 32 TMEM lanes (rows) with tcgen05.ld and write Y[b, row] coalesced (fp32,
 // bf16, or fp32 atomics when K is split).  All waits are bounded; TMEM is always freed.
@@ -507,21 +507,25 @@ cudaError_t launch_fmt(const TcArgs &a, dim3 grid, size_t smem, cudaStream_t st)
 
 }  // namespace
 
-bool tc_supported(const WOperand &w, int64_t B, int)
+// Variant 2: the tensor-memory kernel (k_tc2.cu) where it fits (B <= 256); any other variant: this one.
+bool tc_supported(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
+    if (variant == 2 && tc2_supported(w, B)) return true;
     return encode_fn() != nullptr && tc_shape(w, B, 0, s);
 }
 
-int tc_default_split(const WOperand &w, int64_t B, int)
+int tc_default_split(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
+    if (variant == 2 && tc2_supported(w, B)) return tc2_default_split(w, B);
     return tc_shape(w, B, 0, s) ? s.nsplit : 1;
 }
 
-int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int, float *acc_ws,
-              void *stream)
+int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
+              float *acc_ws, void *stream)
 {
+    if (variant == 2 && tc2_supported(w, B)) return launch_tc2(w, x, B, y, out_bf16, split_k, acc_ws, stream);
     TcShape s;
     if (!tc_shape(w, B, split_k, s)) return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)stream;

@@ -1,7 +1,8 @@
-"""GPU parity of the tcgen05 tensor-core kernel (fused reconstruct into shared memory, fp32 accumulate in
-tensor memory) against the oracle's fp64 contraction: every weight format it consumes (4-bit palette
-codes, exponent bytes, plain bf16 after full decode), ragged N (not a multiple of the 128-row tile),
-batch sizes from 1 to 512 (N-padding, two MMAs per K-step above 256), K-splits and both output dtypes."""
+"""GPU parity of the tcgen05 tensor-core kernels against the oracle's fp64 contraction: variant 0 rebuilds
+into shared memory, variant 2 into tensor memory (the MMA's A operand); both accumulate in fp32 in tensor
+memory.  Every weight format they consume (4-bit palette codes, exponent bytes, plain bf16 after full
+decode), ragged N (not a multiple of the 128-row tile), batch sizes from 1 to 512 (N-padding, two MMAs per
+K-step above 256), K-splits and both output dtypes."""
 import numpy as np
 import pytest
 
@@ -19,26 +20,28 @@ def mats():
     return w, uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN, 256, 12), want_palette_form=True)
 
 
+@pytest.mark.parametrize("variant", [0, 2])
 @pytest.mark.parametrize("B", [1, 3, 16, 17, 100, 256, 300, 512])
 @pytest.mark.parametrize("strategy", [uw.STRAT_DIRECT_PALETTE, uw.STRAT_EXP_ONLY, uw.STRAT_FULL_DECODE,
                                       uw.STRAT_PALETTE_TRANSCODE])
-def test_tc_all_formats(mats, B, strategy):
+def test_tc_all_formats(mats, B, strategy, variant):
     w, m = mats
     x = synth.fill((B, w.shape[1]), seed=B * 13 + strategy)
     yref, absum = oracle.matmul(w, x)
-    y = run_matmul(m, x, (strategy, uw.KERNEL_TC, 1, 0))
+    y = run_matmul(m, x, (strategy, uw.KERNEL_TC, 1, variant))
     ok, worst = tol_ok(y, yref, absum)
     assert ok, worst
 
 
+@pytest.mark.parametrize("variant", [0, 2])
 @pytest.mark.parametrize("split", [2, 3, 16])
 @pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
-def test_tc_splits_and_bf16(mats, split, out_dtype):
+def test_tc_splits_and_bf16(mats, split, out_dtype, variant):
     w, m = mats
     B = 24
     x = synth.fill((B, w.shape[1]), seed=split)
     yref, absum = oracle.matmul(w, x)
-    y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, split, 0), out_dtype)
+    y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, split, variant), out_dtype)
     ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
     assert ok, worst
 
@@ -53,7 +56,8 @@ def test_tc_exact_integers():
     exact = Xi.astype(np.float64) @ Wi.astype(np.float64).T
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
     for s in (uw.STRAT_DIRECT_PALETTE, uw.STRAT_EXP_ONLY, uw.STRAT_FULL_DECODE):
-        assert np.array_equal(run_matmul(m, x, (s, uw.KERNEL_TC, 1, 0)), exact), s
+        for v in (0, 2):
+            assert np.array_equal(run_matmul(m, x, (s, uw.KERNEL_TC, 1, v)), exact), (s, v)
 
 
 @pytest.mark.parametrize("B", [16, 64, 256])
@@ -65,6 +69,7 @@ def test_tc_gate_8b_sampled(B):
     rows = np.unique(np.concatenate([[0, 127, 128, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
     yref, absum = oracle.matmul(w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
-    y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, 0))[:, rows]
-    ok, worst = tol_ok(y, yref, absum)
-    assert ok, worst
+    for v in (0, 2):
+        y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, v))[:, rows]
+        ok, worst = tol_ok(y, yref, absum)
+        assert ok, (v, worst)
