@@ -31,8 +31,22 @@ L2_BYTES = 129 * 2 ** 20
 WORKLOAD = "gate_8b"
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of that kernel as it stands
-# (profiles/gemv_tma_kernel_gate8b_b1.md). Keyed by (workload, batch, kernel name); a kernel change invalidates it.
-MEASURED_TRAFFIC = {("gate_8b", 1, "gemv_tma_kernel"): 91.362816e6}
+# (profiles/launches_bench_gate8b_b1.md, profiles/gemv_mma_kernel_gate8b_b4.md). Keyed by (workload, batch,
+# kernel name); a kernel change invalidates it.
+MEASURED_TRAFFIC = {("gate_8b", 1, "gemv_tma_kernel"): 90.965504e6,
+                    ("gate_8b", 4, "gemv_mma_kernel"): 92.925440e6}
+
+
+def kernel_name(plan, B):
+    """The kernel a plan launches (the dominant kernel of a step), as named in ncu launch lists."""
+    import lossless_bf16_weight_exponent_gb300 as uw
+    if plan.kernel == uw.KERNEL_TC or (plan.kernel == uw.KERNEL_AUTO and B > 16):
+        return "tc2_kernel" if plan.variant == 2 and B <= 256 else "tc_kernel"
+    if plan.variant in (6, 7) and B <= 16:
+        return "gemv_mma_kernel"
+    if plan.variant == 1 or B > 2:
+        return "gemv_kernel"
+    return "gemv_tma_kernel"
 
 
 def parse():
@@ -350,12 +364,7 @@ def run_ours(args):
 
     if rank == 0:
         achieved = alg / (ms_step * 1e-3) / 1e9
-        if plan.kernel == uw.KERNEL_TC or (plan.kernel == uw.KERNEL_AUTO and B > 2):
-            kname = "tc_kernel"
-        elif plan.variant == 1 or B > 2:
-            kname = "gemv_kernel"
-        else:
-            kname = "gemv_tma_kernel"
+        kname = kernel_name(plan, B)
         traffic = MEASURED_TRAFFIC.get((args.workload, B, kname))
         line = {
             "metric": "effective BF16 weight GB/s, fused decompress+matmul (B=%d)" % B,
