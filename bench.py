@@ -64,6 +64,10 @@ def parse():
                    choices=["gate_8b", "down_8b", "gate_70b", "down_70b", "heavy_tail", "tiny"],
                    help="matrix recipe (the JSON line's headline workload is gate_8b)")
     p.add_argument("--plan", default=None, help="force a plan 'strategy,kernel,split,variant' (skips autotuning)")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every configuration (tiny, 8B gate, 8B MLP stack, heavy tail, 70B gate/down) at each of "
+                        "its batch sizes under the autotuned plan; one JSON line per (configuration, B)")
+    p.add_argument("--stack-layers", type=int, default=32, help="layers of the 8B MLP stack in --sweep")
     return p.parse_args()
 
 
@@ -442,10 +446,131 @@ def cpu_baseline(blob, w, mat, B):
             "sample": f"2 full steps: plain-C decode of the Huffman blob + fp64 GEMV at B={B}"}
 
 
+def time_graph(fn, n, reps, stream):
+    """Median µs of one replay of a CUDA graph holding n calls of fn(i, stream), after warm-up replays."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            fn(i, stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i, stream)
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    """Every configuration of the workload list at each of its batch sizes, autotuned plan, graph replays over
+    enough resident copies that a pass streams from HBM (except the tiny matrix, smaller than L2)."""
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    import synth
+    hbm, tf_peak, peak_kind = peaks()
+    stream = torch.cuda.Stream()
+    single = [("tiny", synth.tiny(), [1]), ("gate_8b", synth.gate_8b(), [1, 4, 16]),
+              ("heavy_tail", synth.heavy_tail(), [1, 16, 64]),
+              ("gate_70b", synth.mlp_70b()[0], [1, 32, 256, 512]), ("down_70b", synth.mlp_70b()[2], [1, 32, 256, 512])]
+
+    def line(cfg, mat_desc, B, us, comp_bytes, eff_bytes, flops, plan, extra=None):
+        d = {"config": cfg, "matrix": mat_desc, "B": B, "us": round(us, 2),
+             "compressed_GBps": round(comp_bytes / us / 1e3, 1), "compressed_frac": round(comp_bytes / us / 1e3 / hbm, 3),
+             "effective_GBps": round(eff_bytes / us / 1e3, 1), "effective_frac": round(eff_bytes / us / 1e3 / hbm, 3),
+             "tflops": round(flops / us / 1e6, 1), "tensor_frac": round(flops / us / 1e6 / tf_peak, 3),
+             "plan": plan, "peak_kind": peak_kind}
+        if extra:
+            d.update(extra)
+        print(json.dumps(d), flush=True)
+
+    for cfg, mat, bs in single:
+        blob = uw.encode(mat.weights(), uw.CODEC_HUFFMAN)
+        base = uw.Matrix(blob, want_palette_form=True)
+        info = base.info
+        copies = 1 if cfg == "tiny" else max(2, int(np.ceil(3 * L2_BYTES / info["device_bytes"])))
+        mats = [base] + [uw.Matrix(blob, want_palette_form=True) for _ in range(copies - 1)]
+        need = base.autotune_workspace_size(bs)
+        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        base.autotune(bs, tws, need)
+        del tws
+        table = base.tune_save()
+        for m in mats[1:]:
+            m.tune_load(table)
+        for B in bs:
+            ws_bytes = base.workspace_size(B)
+            ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+            x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+            y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+            n = 32 if copies > 1 else 64
+            us = time_graph(lambda i, s: mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s),
+                            n, 7, stream) / n
+            eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+            line(cfg, f"W[{mat.N},{mat.K}]", B, us, algorithmic_bytes(info, 4, B), eff, 2.0 * B * mat.N * mat.K,
+                 base.plan_for(B).as_tuple(),
+                 {"l2": "matrix smaller than L2" if copies == 1 else f"{copies} copies rotated, inputs larger than L2",
+                  "verbatim_block_fraction": round(info["n_verbatim"] / info["n_blocks"], 4)})
+        del mats, base
+        torch.cuda.empty_cache()
+
+    # 8B MLP stack: gate, up, down per layer, one graph per pass over the whole stack
+    L = args.stack_layers
+    recipes = synth.stack_8b(L)
+    mats, infos, tables = [], [], {}
+    for r in recipes:
+        blob = uw.encode(r.weights(), uw.CODEC_HUFFMAN)
+        m = uw.Matrix(blob, want_palette_form=True)
+        mats.append(m)
+        infos.append(m.info)
+    bs = [1, 8, 32, 128]
+    for shape_first in (0, 2):  # autotune the gate shape and the down shape once, share by shape
+        m0 = mats[shape_first]
+        need = m0.autotune_workspace_size(bs)
+        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        m0.autotune(bs, tws, need)
+        del tws
+        tables[shape_first] = m0.tune_save()
+    for i, m in enumerate(mats):
+        m.tune_load(tables[0 if i % 3 != 2 else 2])
+    for B in bs:
+        ws_bytes = max(m.workspace_size(B) for m in mats[:3])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        x_in = torch.from_numpy(recipes[0].activations(B).view(np.int16)).cuda()            # [B, 4096]
+        x_mid = torch.from_numpy(recipes[2].activations(B).view(np.int16)).cuda()           # [B, 14336]
+        y_mid = torch.empty((B, 14336), dtype=torch.float32, device="cuda")
+        y_out = torch.empty((B, 4096), dtype=torch.float32, device="cuda")
+
+        def call(i, s):
+            m = mats[i]
+            if i % 3 == 2:
+                m.matmul(x_mid, B, y_out, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+            else:
+                m.matmul(x_in, B, y_mid, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+        us = time_graph(call, len(mats), 5, stream)
+        comp = sum(algorithmic_bytes(inf, 4, B) for inf in infos)
+        eff = sum(2 * inf["N"] * inf["K"] + 2 * B * inf["K"] + 4 * B * inf["N"] for inf in infos)
+        flops = sum(2.0 * B * inf["N"] * inf["K"] for inf in infos)
+        line("stack_8b", f"{L} layers x (gate, up W[14336,4096]; down W[4096,14336])", B, us, comp, eff, flops,
+             {"gate_up": mats[0].plan_for(B).as_tuple(), "down": mats[2].plan_for(B).as_tuple()},
+             {"matmuls": len(mats), "us_per_matmul": round(us / len(mats), 2)})
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 

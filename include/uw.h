@@ -107,7 +107,9 @@ typedef struct {
                               *            K a multiple of 256 (6: K-slices of 4096 weights up to B = 8;
                               *            7: of 2048)
                               * UW_KERNEL_TC: 0, 1: rebuilt tiles in shared memory; 2: rebuilt weights in tensor
-                              *   memory (B <= 256)
+                              *   memory (B <= 256); 3: as 2 in a persistent grid that splits the
+                              *   (row tile, 256-weight step) units evenly over the SMs (B <= 256, K a multiple of
+                              *   256, split_k ignored)
                               * a shape that does not fit the matrix or B runs the nearest one that does */
 } uw_plan;
 

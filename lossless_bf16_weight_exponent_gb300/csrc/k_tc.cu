@@ -507,11 +507,13 @@ cudaError_t launch_fmt(const TcArgs &a, dim3 grid, size_t smem, cudaStream_t st)
 
 }  // namespace
 
-// Variant 2: the tensor-memory kernel (k_tc2.cu) where it fits (B <= 256); any other variant: this one.
+// Variant 2: the tensor-memory kernel (k_tc2.cu) where it fits (B <= 256); variant 3: the persistent one
+// (k_tc3.cu, B <= 256, K % 256 == 0); any other variant or shape: this one.
 bool tc_supported(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
     if (variant == 2 && tc2_supported(w, B)) return true;
+    if (variant == 3 && tc3_supported(w, B)) return true;
     return encode_fn() != nullptr && tc_shape(w, B, 0, s);
 }
 
@@ -519,6 +521,7 @@ int tc_default_split(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
     if (variant == 2 && tc2_supported(w, B)) return tc2_default_split(w, B);
+    if (variant == 3 && tc3_supported(w, B)) return 1;
     return tc_shape(w, B, 0, s) ? s.nsplit : 1;
 }
 
@@ -526,6 +529,7 @@ int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_
               float *acc_ws, void *stream)
 {
     if (variant == 2 && tc2_supported(w, B)) return launch_tc2(w, x, B, y, out_bf16, split_k, acc_ws, stream);
+    if (variant == 3 && tc3_supported(w, B)) return launch_tc3(w, x, B, y, out_bf16, acc_ws, stream);
     TcShape s;
     if (!tc_shape(w, B, split_k, s)) return cudaErrorInvalidValue;
     cudaStream_t st = (cudaStream_t)stream;

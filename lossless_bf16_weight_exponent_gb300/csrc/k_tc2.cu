@@ -8,9 +8,9 @@
 // Shared memory then carries only the compressed bytes and the activations.
 //
 // One CTA owns 128 rows of W (the MMA's M) and a range of 64-wide K-stages.
-//   - warp 16 (one thread) TMA-loads compressed stages of 128 weights per row: sign+mantissa [128 x 128] u8
-//     with the 128-byte swizzle and 4-bit codes [128 x 64] u8 with the 64-byte swizzle (or exponent bytes,
-//     or the bf16 tile), so a warp's 32 rows read at once land in distinct bank groups;
+//   - warp 16 (one thread) TMA-loads compressed stages of 256 weights per row as boxes 128 bytes wide with the
+//     128-byte swizzle: sign+mantissa as two [128 x 128] u8 boxes and the 4-bit codes as one (or exponent
+//     bytes, or the bf16 tile), so a warp's 32 rows read at once land in distinct bank groups;
 //   - warp 17 (one thread) TMA-loads the activation tile X [BN x 64] bf16 of each K-stage (128-byte swizzle,
 //     the MMA's K-major B operand);
 //   - warps 0-15 rebuild: warp w belongs to group w / 4, which rebuilds K-stages i = w / 4 (mod 4), and owns
@@ -45,7 +45,7 @@ using namespace dev;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kCK = 128;                      // weights per row in one compressed stage (two K-stages)
+constexpr int kCK = 256;                      // weights per row in one compressed stage (four K-stages)
 constexpr int kGroups = 4;                    // rebuild groups: group q rebuilds K-stages i = q (mod 4)
 constexpr int kRebuildWarps = 4 * kGroups;    // a group has one warp per TMEM lane quarter
 constexpr int kProducerWarp = kRebuildWarps;  // compressed stages
@@ -58,7 +58,7 @@ constexpr int kMaskWords = 8;                 // per-row verbatim masks: up to 2
 
 struct Tc2Args {
     CUtensorMap tm0;   // sm [N, K] u8, box {128, 128}, swizzle 128 B | W bf16 [N, K], box {64, 128}, swizzle 128 B
-    CUtensorMap tm1;   // codes [N, K/2] u8, box {64, 128}, swizzle 64 B | exps [N, K] u8, box {128, 128}, swizzle 128 B
+    CUtensorMap tm1;   // codes [N, K/2] u8, box {128, 128}, swizzle 128 B | exps [N, K] u8, box {128, 128}, swizzle 128 B
     CUtensorMap tm_x;  // X [B, K] bf16, box {64, BN}, swizzle 128 B
     const uint32_t *bitmap, *prefix;
     const uint8_t *verb_exp;
@@ -71,9 +71,9 @@ struct Tc2Args {
 };
 
 template <int FMT> struct CStage;
-template <> struct CStage<FMT_PAL> { static constexpr uint32_t bytes = 128 * 128 + 128 * 64; };
-template <> struct CStage<FMT_EXP> { static constexpr uint32_t bytes = 2 * 128 * 128; };
-template <> struct CStage<FMT_BF16> { static constexpr uint32_t bytes = 2 * 128 * 128; };
+template <> struct CStage<FMT_PAL> { static constexpr uint32_t bytes = 3 * 128 * 128; };   // sm x2, codes
+template <> struct CStage<FMT_EXP> { static constexpr uint32_t bytes = 4 * 128 * 128; };   // sm x2, exps x2
+template <> struct CStage<FMT_BF16> { static constexpr uint32_t bytes = 4 * 128 * 128; };  // bf16 x4
 
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) tc2_kernel(const __grid_constant__ Tc2Args a)
@@ -108,14 +108,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc2_kernel(const __grid_constant_
     const int64_t row0 = (int64_t)blockIdx.x * BM;
     const int k_stage0 = blockIdx.y * a.ks_stages;
     const int nks = (int)min((int64_t)a.ks_stages, K / BK - k_stage0);
-    const int ncs = (nks + 1) / 2;
+    const int ncs = (nks + 3) / 4;
     const uint32_t x_bytes = (uint32_t)a.BN * 128;
 
     if (FMT == FMT_PAL) fill_pair_table(tab, a.palette, threadIdx.x, blockDim.x);
     if (threadIdx.x == 0) {
         for (int s = 0; s < SC; s++) {
             mbar_init(&cfull[s], 1);
-            mbar_init(&cempty[s], 8);  // the two groups of its K-stages, four warps each
+            mbar_init(&cempty[s], 16);  // the four groups of its K-stages, four warps each
         }
         for (int s = 0; s < SX; s++) {
             mbar_init(&xfull[s], 1);
@@ -151,11 +151,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc2_kernel(const __grid_constant_
                 const int kw = k_stage0 * BK + c * kCK;  // first weight of the stage
                 mbar_expect_tx(&cfull[s], CStage<FMT>::bytes);
                 if (FMT == FMT_BF16) {
-                    tma2d(st, &a.tm0, kw, (int)row0, &cfull[s]);
-                    tma2d(st + 128 * 128, &a.tm0, kw + BK, (int)row0, &cfull[s]);
+#pragma unroll
+                    for (int j = 0; j < 4; j++) tma2d(st + j * 16384, &a.tm0, kw + j * BK, (int)row0, &cfull[s]);
                 } else {
                     tma2d(st, &a.tm0, kw, (int)row0, &cfull[s]);
-                    tma2d(st + 128 * 128, &a.tm1, FMT == FMT_PAL ? kw / 2 : kw, (int)row0, &cfull[s]);
+                    tma2d(st + 16384, &a.tm0, kw + 128, (int)row0, &cfull[s]);
+                    if (FMT == FMT_PAL) tma2d(st + 32768, &a.tm1, kw / 2, (int)row0, &cfull[s]);
+                    else {
+                        tma2d(st + 32768, &a.tm1, kw, (int)row0, &cfull[s]);
+                        tma2d(st + 49152, &a.tm1, kw + 128, (int)row0, &cfull[s]);
+                    }
                 }
                 issued = c + 1;
             }
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc2_kernel(const __grid_constant_
         }
         const uint32_t t_lane = (uint32_t)(32 * quarter) << 16;
         for (int i = group; i < nks; i += kGroups) {
-            const int c = i >> 1, sub = i & 1, cs = c % SC, sa = i % SA;
+            const int c = i >> 2, sub = i & 3, cs = c % SC, sa = i % SA;
             if (!mbar_wait(&cfull[cs], (c / SC) & 1)) { ok = false; break; }
             const uint8_t *cst = cring + (size_t)cs * a.cstage_bytes;
             uint4 d0[4], d1[4];  // PAL: sm pieces, codes (d1[0..1]); EXP: sm, exps; BF16: the 8 pieces
@@ -288,16 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc2_kernel(const __grid_constant_
                     d1[p] = *(const uint4 *)(cst + sub * 16384 + r * 128 + (((p + 4) ^ (r & 7)) << 4));
                 }
             } else {
+                // sm box h = sub / 2 holds K-stages 2h, 2h + 1: this one is its half q = sub % 2
+                const int h = sub >> 1, q = sub & 1;
 #pragma unroll
-                for (int p = 0; p < 4; p++) d0[p] = *(const uint4 *)(cst + r * 128 + (((4 * sub + p) ^ (r & 7)) << 4));
+                for (int p = 0; p < 4; p++)
+                    d0[p] = *(const uint4 *)(cst + h * 16384 + r * 128 + (((4 * q + p) ^ (r & 7)) << 4));
                 if (FMT == FMT_PAL) {
+                    // the codes box holds all four K-stages: 32 code bytes each
 #pragma unroll
                     for (int p = 0; p < 2; p++)
-                        d1[p] = *(const uint4 *)(cst + 16384 + r * 64 + (((2 * sub + p) ^ ((r >> 1) & 3)) << 4));
+                        d1[p] = *(const uint4 *)(cst + 32768 + r * 128 + (((2 * sub + p) ^ (r & 7)) << 4));
                 } else {
 #pragma unroll
                     for (int p = 0; p < 4; p++)
-                        d1[p] = *(const uint4 *)(cst + 16384 + r * 128 + (((4 * sub + p) ^ (r & 7)) << 4));
+                        d1[p] = *(const uint4 *)(cst + 32768 + h * 16384 + r * 128 + (((4 * q + p) ^ (r & 7)) << 4));
                 }
             }
             __syncwarp();
@@ -426,11 +435,11 @@ bool tc2_shape(const WOperand &w, int64_t B, int split_k, Tc2Shape &s)
     s.acol0 = (s.BN + 31) / 32 * 32;
     s.aslots = std::min(8, (kTmemCols - s.acol0) / 32);
     s.cstage_bytes = w.fmt == FMT_PAL ? (int)CStage<FMT_PAL>::bytes : (int)CStage<FMT_EXP>::bytes;
-    // activation tiles are small but each carries a full memory latency: keep ~64 KB of them in flight
-    s.xstages = std::max(2, std::min(32, (64 * 1024) / (s.BN * 128)));
+    // activation tiles are small but each carries a full memory latency: keep ~16 KB of them in flight
+    s.xstages = std::max(2, std::min(8, (16 * 1024) / (s.BN * 128)));
     const size_t cap = 227 * 1024;
     const bool pal = w.fmt == FMT_PAL;
-    s.vcap = pal ? 256 : 0;
+    s.vcap = pal ? 128 : 0;
     const size_t vbytes = pal ? (size_t)(2 * kMaskWords * BM + 2 * BM) * 4 + (size_t)s.vcap * 64 : 0;
     const size_t fixed = 1024 /* alignment slack */ + (pal ? kPairTableBytes : 0) + 1024 + (vbytes + 1023) / 1024 * 1024 +
                          (size_t)s.xstages * s.BN * 128;
@@ -500,7 +509,7 @@ int launch_tc2(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
     } else {
         ok &= make_map2d(&a.tm0, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.sm, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         if (w.fmt == FMT_PAL)
-            ok &= make_map2d(&a.tm1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+            ok &= make_map2d(&a.tm1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
         else
             ok &= make_map2d(&a.tm1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.exps, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     }

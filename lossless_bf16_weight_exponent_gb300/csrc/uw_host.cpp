@@ -449,6 +449,39 @@ uw_status parse_and_validate(const uint8_t *p, size_t size, BlobHeader *out, boo
     return UW_OK;
 }
 
+void build_tile_verbatim(const BlobHeader &h, const uint8_t *blob, std::vector<uint32_t> &off,
+                         std::vector<uint32_t> &mask, std::vector<uint8_t> &data)
+{
+    const int64_t N = h.N, K = h.K, KB = K / 64;
+    const int64_t tiles = (N + 127) / 128, upk = K / 256, units = tiles * upk;
+    const uint32_t *bm = (const uint32_t *)(blob + h.off[S_BITMAP]);
+    const uint32_t *pf = (const uint32_t *)(blob + h.off[S_PREFIX]);
+    const uint8_t *ve = blob + h.off[S_VERB];
+    off.assign((size_t)units + 1, 0);
+    mask.assign((size_t)units * 16, 0);
+    data.clear();
+    data.reserve((size_t)h.n_verbatim * 64);
+    uint32_t cnt = 0;
+    for (int64_t t = 0; t < tiles; t++)
+        for (int64_t kq = 0; kq < upk; kq++) {
+            const int64_t u = t * upk + kq;
+            off[(size_t)u] = cnt;
+            for (int j = 0; j < 4; j++)
+                for (int r = 0; r < 128; r++) {
+                    const int64_t row = t * 128 + r;
+                    if (row >= N) break;
+                    const uint64_t b = (uint64_t)row * (uint64_t)KB + (uint64_t)(kq * 4 + j);
+                    const uint32_t w = bm[b >> 5];
+                    if (!((w >> (b & 31)) & 1u)) continue;
+                    mask[(size_t)u * 16 + 4 * j + (r >> 5)] |= 1u << (r & 31);
+                    const uint64_t vi = pf[b >> 5] + (uint64_t)__builtin_popcount(w & ((1u << (b & 31)) - 1u));
+                    data.insert(data.end(), ve + vi * 64, ve + vi * 64 + 64);
+                    cnt++;
+                }
+        }
+    off[(size_t)units] = cnt;
+}
+
 }  // namespace uw
 
 extern "C" const char *uw_status_string(uw_status s)

@@ -38,6 +38,10 @@ void canonical_codes(const uint8_t *lens, uint32_t *codes);
 void build_decode_table(const uint8_t *lens, int max_len, std::vector<uint8_t> &table);
 // Multi-symbol table over 12-bit windows (limits <= 12), see uw_host.cpp for the entry layout.
 void build_multi_table(const uint8_t *lens, std::vector<uint32_t> &table);
+// Tile-major verbatim stream of a blob (K % 256 == 0): per unit of 128 rows x 256 weights, a 16-word mask
+// ([K-stage j][row word]) and the count prefix; the verbatim exponents reordered unit by unit, (j, row) order.
+void build_tile_verbatim(const BlobHeader &h, const uint8_t *blob, std::vector<uint32_t> &off,
+                         std::vector<uint32_t> &mask, std::vector<uint8_t> &data);
 
 // --------------------------------------------------------------------------------------------
 // Device view of a loaded matrix (plain pointers, passed by value to kernels).
@@ -76,6 +80,11 @@ struct WOperand {
     const uint16_t *w;        // FMT_BF16: [N*K]
     const uint32_t *bitmap, *prefix;
     const uint8_t *verb_exp;  // FMT_PAL verbatim handling
+    // tile-major verbatim stream (present when K % 256 == 0): for unit u = tile * (K / 256) + kq (128 rows x 256
+    // weights), tmv_mask[16u + 4j + w] bit b = row 32w + b's block kq*4 + j is verbatim; its exponents follow
+    // those of earlier (j, row) in the unit at tmv_data[64 * (tmv_off[u] + rank)]
+    const uint32_t *tmv_off, *tmv_mask;
+    const uint8_t *tmv_data;
     uint8_t palette[16];
     int64_t N, K;
     int *status;              // device status word of the matrix
@@ -106,6 +115,9 @@ bool tc2_supported(const WOperand &w, int64_t B);
 int tc2_default_split(const WOperand &w, int64_t B);
 int launch_tc2(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, float *acc_ws,
                void *stream);
+// persistent tcgen05 GEMM (one CTA per SM over balanced 128 x 256 units; B <= 256, K % 256 == 0): variant 3
+bool tc3_supported(const WOperand &w, int64_t B);
+int launch_tc3(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
 int gemv_default_split(const WOperand &w, int64_t B);
 int tc_default_split(const WOperand &w, int64_t B, int variant);
 int num_sms();

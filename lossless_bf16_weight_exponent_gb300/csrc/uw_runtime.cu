@@ -44,6 +44,8 @@ struct uw_matrix {
     void *dev = nullptr;
     size_t dev_bytes = 0;
     uint8_t *codes = nullptr;  // resident 4-bit codes (may be null for Huffman)
+    const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
+    const uint8_t *tmv_data = nullptr;
     int device = 0;
     std::mutex mu;
     std::vector<TuneEntry> tune;
@@ -108,6 +110,14 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     const bool multi = h.codec == UW_CODEC_HUFFMAN && h.max_len <= 12;
     const uint64_t o_mtab = multi ? take(4096 * 4) : 0;
     const uint64_t o_st = take(256);
+    // tile-major verbatim stream for the tcgen05 kernels (units of 128 rows x 256 weights)
+    std::vector<uint32_t> tmv_off, tmv_mask;
+    std::vector<uint8_t> tmv_data;
+    const bool tmv = h.K % 256 == 0 && h.N > 0;
+    if (tmv) build_tile_verbatim(h, p, tmv_off, tmv_mask, tmv_data);
+    const uint64_t o_tmo = tmv ? take(tmv_off.size() * 4 + 16) : 0;
+    const uint64_t o_tmm = tmv ? take(tmv_mask.size() * 4 + 16) : 0;
+    const uint64_t o_tmd = tmv ? take(tmv_data.size() + 64) : 0;
 
     uw_matrix *m = new (std::nothrow) uw_matrix();
     if (!m) return fail(UW_ERR_NO_MEMORY, "uw_load: host allocation");
@@ -128,6 +138,11 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
         (resident_codes && h.codec == UW_CODEC_PALETTE && (e = up(o_codes, S_IDX))) || (e = up(o_co, S_CHUNK)) ||
         (e = up(o_bits, S_BITS)))
         return fail_free(cuda_fail(e, "uw_load: upload"));
+    if (tmv && ((e = cudaMemcpyAsync(d + o_tmo, tmv_off.data(), tmv_off.size() * 4, cudaMemcpyHostToDevice, st)) ||
+                (e = cudaMemcpyAsync(d + o_tmm, tmv_mask.data(), tmv_mask.size() * 4, cudaMemcpyHostToDevice, st)) ||
+                (!tmv_data.empty() &&
+                 (e = cudaMemcpyAsync(d + o_tmd, tmv_data.data(), tmv_data.size(), cudaMemcpyHostToDevice, st)))))
+        return fail_free(cuda_fail(e, "uw_load: verbatim stream upload"));
     std::vector<uint8_t> table;
     std::vector<uint32_t> mtable;
     if (h.codec == UW_CODEC_HUFFMAN) {
@@ -156,6 +171,9 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     v.dtab = d + o_tab;
     v.mtab = multi ? (const uint32_t *)(d + o_mtab) : nullptr;
     v.status = (int *)(d + o_st);
+    m->tmv_off = tmv ? (const uint32_t *)(d + o_tmo) : nullptr;
+    m->tmv_mask = tmv ? (const uint32_t *)(d + o_tmm) : nullptr;
+    m->tmv_data = tmv ? d + o_tmd : nullptr;
     if (h.codec == UW_CODEC_HUFFMAN && want_palette_form) {
         if ((e = (cudaError_t)launch_decode_huffman(v, DEC_CODES, m->codes, st)))
             return fail_free(cuda_fail(e, "uw_load: palette transcode"));
@@ -264,6 +282,9 @@ static WOperand operand_shape(const uw_matrix *m, int strategy)
     w.bitmap = m->v.bitmap;
     w.prefix = m->v.prefix;
     w.verb_exp = m->v.verb_exp;
+    w.tmv_off = m->tmv_off;
+    w.tmv_mask = m->tmv_mask;
+    w.tmv_data = m->tmv_data;
     w.codes = m->codes;
     w.status = m->v.status;
     return w;
