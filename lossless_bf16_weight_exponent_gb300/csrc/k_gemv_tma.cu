@@ -18,7 +18,12 @@
 // free.  A consumer copies its part of a stage into registers and releases the
 // slot before computing on it.  Two 4-bit codes (one code byte) select the
 // exponent fields of a bf16x2 pair from a 32 KB per-lane table in shared memory,
-// so a warp's lookups never share a bank.  Lane sums of four consecutive stages
+// so a warp's lookups never share a bank.  A stage without verbatim blocks runs a
+// straight-line body; a verbatim block's codes are all zero, so reading a zero table
+// row under a zero sign+mantissa mask makes it add exactly +0 * x, and after the main
+// loop the consumers add the CTA's verbatim blocks' true products (their exponents,
+// sign+mantissa bytes and X from global memory) - no warp runs a slower body that
+// would hold the ring back.  Lane sums of four consecutive stages
 // are reduced together (a transposed butterfly), and row sums meet in shared
 // memory and are written once at the end.  Every
 // mbarrier wait is bounded by a global-timer limit; on expiry the kernel latches
@@ -30,6 +35,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "uw_internal.h"
 
@@ -59,7 +65,6 @@ struct TmaArgs {  // 64-byte aligned through its tensor maps
     int stage_bytes; // bytes of one stage
     int rows_cta;    // max rows owned by one CTA
     int bm_words;    // max verbatim-bitmap words of one CTA's rows
-    int vcap;        // verbatim blocks of the CTA's rows staged in shared memory (beyond: global loads)
     int w_from_prev; // the weight stream is written by the preceding kernel (a preprocess workspace)
     int *status;
 };
@@ -217,17 +222,70 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     uint8_t *tab = smem;                                                      // [TB] pair table
     uint64_t *full = (uint64_t *)(smem + TB);                                 // [stages]
     uint64_t *empty = full + a.stages;                                        // [stages]
-    uint64_t *vfull = empty + a.stages;                                       // staged verbatim exponents landed
+    uint8_t *zrow = smem + TB + 512;                                          // [128] zeros: verbatim groups' table row
     float *part = (float *)(smem + TB + 1024);                                // [rows_cta][NB]
     const int part_bytes = (a.rows_cta * NB * 4 + 1023) / 1024 * 1024;
     const int bm_bytes = (a.bm_words * 4 + 1023) / 1024 * 1024;
     uint32_t *bm = (uint32_t *)(smem + TB + 1024 + part_bytes);              // [bm_words] bitmap
     uint32_t *pf = (uint32_t *)(smem + TB + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
-    uint8_t *vx = smem + TB + 1024 + part_bytes + 2 * bm_bytes;              // [vcap][64] verbatim exps
-    uint8_t *ring = vx + ((size_t)a.vcap * 64 + 1023) / 1024 * 1024;  // 1024-aligned: tensor copies want 128
+    uint8_t *ring = smem + TB + 1024 + part_bytes + 2 * bm_bytes;            // 1024-aligned: tensor copies want 128
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = a.rs * a.wk;  // consumer warps
+    const int CT = C * 32;
+
+    // Verbatim blocks.  The main loop counts each as exactly zero, so no consumer warp runs a slower body for them
+    // and holds up the ring; this pass, run by the consumers after the main loop, adds their true products into the
+    // row sums.  (Run before the main loop it delays the first stages; run by the producer warp once it has issued
+    // every stage it is one warp doing serial round trips: both measured slower.)  The CTA's verbatim blocks are
+    // ranks [v_begin, v_end) of the verbatim stream; thread `tid` of `nt` takes every nt-th rank (the word holding
+    // a rank by binary search of the prefix counts) and reads the block's bytes and X from global memory.
+    auto verbatim_products = [&](int tid, int nt) {
+        if (FMT != FMT_PAL || !nrows) return;
+        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64, kpr = (uint64_t)K / 64;
+        const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
+        const uint64_t lw = (lb >> 5) - wb0;
+        const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
+                                                    : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
+        for (uint64_t v = v_begin + tid; v < v_end; v += nt) {
+            int lo = 0, hi = n_bw - 1;  // the last word whose prefix count is <= v
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if ((uint64_t)pf[mid] <= v) lo = mid;
+                else hi = mid - 1;
+            }
+            const int bit = (int)__fns(bm[lo], 0, (int)(v - pf[lo]) + 1);
+            const uint64_t blk = (wb0 + lo) * 32 + (uint32_t)bit;
+            const uint32_t row = (uint32_t)blk / (uint32_t)kpr;  // (blocks of a matrix fit 32 bits)
+            const int64_t kb = (int64_t)((uint32_t)blk - row * (uint32_t)kpr) * 64;
+            if (bit > 31 || kb < k0 || kb >= k0 + klen) continue;  // another K-slice's block
+            float sum[NB];
+#pragma unroll
+            for (int j = 0; j < NB; j++) sum[j] = 0.f;
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const uint4 ev = __ldg((const uint4 *)(a.w.verb_exp + v * 64 + 16 * p));
+                const uint4 sv = __ldg((const uint4 *)(a.w.sm + blk * 64 + 16 * p));
+#pragma unroll
+                for (int j = 0; j < NB; j++) {
+                    if (b0 + j >= a.B) continue;
+                    const uint4 *xp = (const uint4 *)(a.x + (b0 + j) * K + kb + 16 * p);
+                    const uint4 xa = __ldg(xp), xb = __ldg(xp + 1);
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        uint32_t p01, p23;
+                        pairs_from_exps(word_of(sv, q), word_of(ev, q), p01, p23);
+                        const uint4 &xv = q < 2 ? xa : xb;
+                        sum[j] = fma2_bf16(p01, word_of(xv, 2 * (q & 1)), sum[j]);
+                        sum[j] = fma2_bf16(p23, word_of(xv, 2 * (q & 1) + 1), sum[j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < NB; j++)
+                if (b0 + j < a.B) atomicAdd(&part[(row - r0) * NB + j], sum[j]);
+        }
+    };
     if (threadIdx.x == 0) {
         if (a.tmap) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tm0) : "memory");
@@ -237,7 +295,6 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C);
         }
-        mbar_init(vfull, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -249,32 +306,11 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         // ------------------------------------------------------------ producer
         // lane 0 runs the ring's barriers; lane r issues the copies of row r of each stage, so a stage's copies
         // leave in one warp instruction rather than one after another
-        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;  // first block, one past last
         if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
         int issued = 0;
         bool ok = true;
-        bool verb_issued = FMT != FMT_PAL;
         for (int i = 0; i < n_stages; i++) {
             const int slot = i % a.stages;
-            if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
-                // the ring is primed: stage the CTA's verbatim blocks, one contiguous run [v_begin, v_end) of the
-                // verbatim stream
-                if (lane == 0) {
-                    uint32_t v_staged = 0;
-                    uint64_t v_begin = 0;
-                    if (nrows) {
-                        const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
-                        const uint32_t bw0 = __ldg(a.w.bitmap + (fb >> 5)), pw0 = __ldg(a.w.prefix + (fb >> 5));
-                        const uint32_t bw1 = __ldg(a.w.bitmap + lwd), pw1 = __ldg(a.w.prefix + lwd);
-                        v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
-                        const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
-                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
-                    }
-                    mbar_arrive_expect_tx(vfull, v_staged * 64);
-                    if (v_staged) bulk_g2s(vx, a.w.verb_exp + v_begin * 64, v_staged * 64, vfull);
-                }
-                verb_issued = true;
-            }
             const int64_t g0 = r0 + (int64_t)i * a.rs;
             const int nr = (int)min((int64_t)a.rs, r1 - g0);
             const bool whole = a.tmap && nr == a.rs && klen == a.ks;  // one tensor copy per stream: the whole stage
@@ -309,10 +345,6 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             issued = i + 1;
         }
         if (lane == 0) {
-            if (!verb_issued) mbar_arrive_expect_tx(vfull, 0);  // no stages (or a timeout before priming)
-            // consumers wait for the staged verbatim run only when they meet a verbatim block: make sure the
-            // copy has landed before the CTA can exit
-            if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
             if (!ok) {
                 atomicExch(a.status, (int)DEV_TIMEOUT);
                 // drain: every issued stage's copies must land before the CTA may exit
@@ -325,25 +357,28 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     // ---------------------------------------------------------------- consumers
     const int ctid = threadIdx.x - 32;
     if (FMT == FMT_PAL)
-        for (int i = ctid; i < a.bm_words; i += C * 32) {  // words past the CTA's blocks read as "not verbatim"
+        for (int i = ctid; i < a.bm_words; i += CT) {  // words past the CTA's blocks read as "not verbatim"
             bm[i] = i < n_bw ? __ldg(a.w.bitmap + wb0 + i) : 0u;
             pf[i] = i < n_bw ? __ldg(a.w.prefix + wb0 + i) : 0u;
         }
-    for (int i = ctid; i < a.rows_cta * NB; i += C * 32) part[i] = 0.f;
+    for (int i = ctid; i < a.rows_cta * NB; i += CT) part[i] = 0.f;
+    if (ctid < 32) ((uint32_t *)zrow)[ctid] = 0u;
     const int c = warp - 1;
     const int slot_row = c / a.wk, piece = c % a.wk;
     const int kbase = piece * 32 * LW + 16 * lane;
     if (FMT == FMT_PAL) {
         // entry row b holds the pair for code byte b once per lane: consecutive threads store consecutive
         // 16-byte chunks (bank-conflict free)
-        for (int i = ctid; i < 256 * 8; i += C * 32) {
+        for (int i = ctid; i < 256 * 8; i += CT) {
             const int b = i >> 3, q = i & 7;
             const uint32_t v = ((uint32_t)a.w.palette[b >> 4] << 23) | ((uint32_t)a.w.palette[b & 15] << 7);
             *(uint4 *)(tab + 128 * b + 16 * q) = make_uint4(v, v, v, v);
         }
     }
-    const uint8_t *tab_lane = tab + 4 * lane;
     grid_dependency_wait();   // X (and Y, written below) belong to the stream order after the preceding kernel
+    const uint8_t *tab_lane = tab + 4 * lane;
+    const uint8_t *zero_lane = zrow + 4 * lane;
+    asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // bitmap words and zeroed row sums are in place
     uint32_t xr[NB][LW / 2];  // bf16x2 activations of the lane's weights
 #pragma unroll
     for (int j = 0; j < NB; j++)
@@ -362,13 +397,12 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 xr[j][8 * g + 4 + q] = word_of(hi, q);
             }
         }
-    asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");  // bitmap words and zeroed row sums are in place
     // block index of the lane's first group in the first stage, relative to the CTA's first bitmap word
-    const uint64_t blk_lane0 = (((uint64_t)(r0 + slot_row) * K + k0 + kbase) >> 6) - wb0 * 32;
-    const uint64_t blk_stage = (uint64_t)a.rs * K / 64;
-    bool ok = true, vx_ready = false;
-    uint64_t v_begin = 0;
-    uint32_t v_staged = 0;
+    // (32-bit: a CTA's blocks number far fewer than 2^32), advanced by one stage of rows per stage
+    uint32_t bl_lane = (uint32_t)((((uint64_t)(r0 + slot_row) * K + k0 + kbase) >> 6) - wb0 * 32);
+    const uint32_t bl_step = (uint32_t)((uint64_t)a.rs * K / 64);
+    const bool all_groups = kbase + 512 * (G - 1) < klen;  // every group of the lane lies inside the K-slice
+    bool ok = true;
     float vs[4][NB];  // lane sums of the last four stages, oldest first, awaiting one joint reduction
 #pragma unroll
     for (int q = 0; q < 4; q++)
@@ -410,9 +444,9 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         }
         // verbatim flags of the lane's groups this stage: bit 8g of `vwin` (groups are 8 blocks apart)
         uint64_t vwin = 0;
-        uint32_t bl0 = 0;
+        const uint32_t bl0 = bl_lane;
+        bl_lane += bl_step;
         if (FMT == FMT_PAL && live) {
-            bl0 = (uint32_t)(blk_lane0 + i * blk_stage);
             if (G <= 4) {
                 const uint64_t w2 = ((uint64_t)bm[(bl0 >> 5) + 1] << 32) | bm[bl0 >> 5];
                 vwin = (w2 >> (bl0 & 31)) & (G == 1 ? 0x1ull : G == 2 ? 0x101ull : 0x01010101ull);
@@ -432,58 +466,54 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         float acc0[NB], acc1[NB];
 #pragma unroll
         for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
+        // The lane's groups of this stage.  BD: some group of the warp lies past the CTA's rows or the K-slice
+        // (those are skipped).  VB: some lane of the warp has a verbatim group; a verbatim group (its codes are
+        // all zero) reads a zero table row under a zero sign+mantissa mask, so it adds exactly +0 * x (the
+        // verbatim warp adds its true product).  Without BD the groups are straight-line code.
+        auto run_groups = [&](auto BD, auto VB) {
+            constexpr bool bd = decltype(BD)::value, vb = decltype(VB)::value;
 #pragma unroll
-        for (int g = 0; g < G; g++) {
-            if (!live || kbase + 512 * g >= klen) continue;  // past the CTA's rows or the K-slice
-            if (!kEarly) load_group(g, d0[g], d1[g]);
-            uint32_t pw[8];  // 8 bf16x2 pairs of weights
-            if (FMT == FMT_PAL) {
-                if (__builtin_expect(vwin != 0, 0) && ((vwin >> (8 * g)) & 1u)) {
-                    if (!vx_ready) {  // first verbatim block of this warp: the staged run must have landed
-                        if (!mbar_wait(vfull, 0)) ok = false;
-                        const uint64_t fb = (uint64_t)r0 * K / 64;
-                        const uint32_t w0 = bm[0];
-                        v_begin = pf[0] + __popc(w0 & ((1u << (fb & 31)) - 1u));
-                        const uint64_t lb = (uint64_t)r1 * K / 64, lw = lb >> 5;
-                        const uint64_t v_end = lw - wb0 < (uint64_t)n_bw
-                                                   ? pf[lw - wb0] + __popc(bm[lw - wb0] & ((1u << (lb & 31)) - 1u))
-                                                   : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
-                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
-                        vx_ready = true;
-                    }
-                    const uint32_t bl = bl0 + 8 * g;
-                    const uint32_t bw = bm[bl >> 5];
-                    const uint64_t vi = pf[bl >> 5] + __popc(bw & ((1u << (bl & 31)) - 1u));
-                    const uint64_t vl = vi - v_begin;
-                    const int within = (kbase + 512 * g) & 63;
-                    const uint4 ev = vl < (uint64_t)v_staged ? *(const uint4 *)(vx + vl * 64 + within)
-                                                              : __ldg((const uint4 *)(a.w.verb_exp + vi * 64 + within));
-#pragma unroll
-                    for (int q = 0; q < 4; q++) pairs_from_exps(word_of(d0[g], q), word_of(ev, q), pw[2 * q], pw[2 * q + 1]);
-                } else {
+            for (int g = 0; g < G; g++) {
+                if (bd && (!live || kbase + 512 * g >= klen)) continue;  // past the CTA's rows or the K-slice
+                if (!kEarly) load_group(g, d0[g], d1[g]);
+                uint32_t pw[8];  // 8 bf16x2 pairs of weights
+                if (FMT == FMT_PAL) {
+                    const bool vg = vb && ((vwin >> (8 * g)) & 1u);
+                    const uint8_t *tl = vg ? zero_lane : tab_lane;
+                    const uint32_t msk = vg ? 0u : 0x807F807Fu;
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const uint32_t S = word_of(d0[g], q);
                         const uint32_t Cw = q < 2 ? d1[g].x : d1[g].y;
                         const int jb = 2 * (q & 1);
-                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb);
-                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb + 1);
+                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & msk) | pair_exp(tl, Cw, jb);
+                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & msk) | pair_exp(tl, Cw, jb + 1);
                     }
+                } else if (FMT == FMT_EXP) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        pairs_from_exps(word_of(d0[g], q), word_of(d1[g], q), pw[2 * q], pw[2 * q + 1]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[g], q); pw[4 + q] = word_of(d1[g], q); }
                 }
-            } else if (FMT == FMT_EXP) {
 #pragma unroll
-                for (int q = 0; q < 4; q++) pairs_from_exps(word_of(d0[g], q), word_of(d1[g], q), pw[2 * q], pw[2 * q + 1]);
-            } else {
+                for (int j = 0; j < NB; j++)
 #pragma unroll
-                for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[g], q); pw[4 + q] = word_of(d1[g], q); }
+                    for (int t = 0; t < 8; t += 2) {
+                        acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
+                        acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
+                    }
             }
-#pragma unroll
-            for (int j = 0; j < NB; j++)
-#pragma unroll
-                for (int t = 0; t < 8; t += 2) {
-                    acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
-                    acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
-                }
+        };
+        // the votes are warp-uniform: every lane of the warp takes the same body
+        const unsigned am = __activemask();
+        const bool bd = !__all_sync(am, live && all_groups), vb = FMT == FMT_PAL && __any_sync(am, vwin != 0);
+        if (!bd) {
+            if (!vb) run_groups(std::false_type{}, std::false_type{});
+            else run_groups(std::false_type{}, std::true_type{});
+        } else {
+            run_groups(std::true_type{}, std::true_type{});
         }
         if (!kEarly) {
             __syncwarp();
@@ -511,8 +541,9 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             }
         }
     }
+    verbatim_products(ctid, CT);
     if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
-    asm volatile("bar.sync 1, %0;" ::"r"(C * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // row sums complete
     // write the CTA's rows
     for (int i = ctid; i < nrows * NB; i += C * 32) {
         const int rl = i / NB, j = i - rl * NB;
@@ -557,7 +588,7 @@ cudaError_t launch_lw(int fmt, const TmaArgs &a, dim3 grid, int threads, size_t 
 }
 
 struct TmaShape {
-    int nsplit, ks, lw, wk, rs, stages, stage_bytes, rows_cta, bm_words, vcap, ctas;
+    int nsplit, ks, lw, wk, rs, stages, stage_bytes, rows_cta, bm_words, ctas;
     size_t smem;
 };
 
@@ -595,11 +626,8 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     s.ctas = (int)std::min<int64_t>(s.ctas, (w.N + s.rs - 1) / s.rs);
     s.rows_cta = (int)((w.N + s.ctas - 1) / s.ctas) + 1;
     s.bm_words = (int)((int64_t)s.rows_cta * (w.K / 64) / 32 + 2);
-    // staged verbatim blocks: up to ~3% of the CTA's blocks, at most 4 KB (the rest use global loads)
-    const int64_t cta_blocks = (int64_t)s.rows_cta * (w.K / 64);
-    s.vcap = w.fmt == FMT_PAL ? (int)std::min<int64_t>(64, std::max<int64_t>(16, cta_blocks * 3 / 100)) : 0;
     const size_t fixed = (w.fmt == FMT_PAL ? kTableBytes : 0) + 1024 + ((size_t)s.rows_cta * nb * 4 + 1023) / 1024 * 1024 +
-                         2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024) + ((size_t)s.vcap * 64 + 1023) / 1024 * 1024;
+                         2 * (((size_t)s.bm_words * 4 + 1023) / 1024 * 1024);
     if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
     s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);
     s.smem = fixed + (size_t)s.stages * s.stage_bytes;
@@ -694,7 +722,6 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
     a.stage_bytes = s.stage_bytes;
     a.rows_cta = s.rows_cta;
     a.bm_words = s.bm_words;
-    a.vcap = s.vcap;
     a.w_from_prev = w.w_from_prev;
     a.status = status;
     a.tmap = make_stage_maps(w, s, a.tm0, a.tm1) ? 1 : 0;
