@@ -116,6 +116,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// L2 policies: the weight streams are read once per launch (evict first); X is read again by the verbatim pass at
+// the end of the launch (evict last)
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ldg_hint(const void *src, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(src), "l"(pol));
+    return v;
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -124,12 +149,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar)
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar, uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
-            "r"(smem_addr(dst)),
-        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, "
+        "%4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
 }
 
@@ -241,6 +274,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     // ranks [v_begin, v_end) of the verbatim stream; thread `tid` of `nt` takes every nt-th rank (the word holding
     // a rank by binary search of the prefix counts) and reads the block's bytes and X from global memory.
     auto verbatim_products = [&](int tid, int nt) {
+        const uint64_t pol_x = l2_evict_last();
         if (FMT != FMT_PAL || !nrows) return;
         const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64, kpr = (uint64_t)K / 64;
         const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
@@ -270,7 +304,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 for (int j = 0; j < NB; j++) {
                     if (b0 + j >= a.B) continue;
                     const uint4 *xp = (const uint4 *)(a.x + (b0 + j) * K + kb + 16 * p);
-                    const uint4 xa = __ldg(xp), xb = __ldg(xp + 1);
+                    const uint4 xa = ldg_hint(xp, pol_x), xb = ldg_hint(xp + 1, pol_x);
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         uint32_t p01, p23;
@@ -307,6 +341,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         // lane 0 runs the ring's barriers; lane r issues the copies of row r of each stage, so a stage's copies
         // leave in one warp instruction rather than one after another
         if (a.w_from_prev) grid_dependency_wait();  // the workspace is written by the preceding kernel
+        const uint64_t pol_w = l2_evict_first();
         int issued = 0;
         bool ok = true;
         for (int i = 0; i < n_stages; i++) {
@@ -321,10 +356,10 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 else {
                     mbar_arrive_expect_tx(&full[slot], wbytes * nr);
                     if (whole) {
-                        if (FMT == FMT_BF16) tma3d(st, &a.tm0, 0, (int)(k0 >> 10), (int)g0, &full[slot]);
+                        if (FMT == FMT_BF16) tma3d(st, &a.tm0, 0, (int)(k0 >> 10), (int)g0, &full[slot], pol_w);
                         else {
-                            tma3d(st, &a.tm0, 0, (int)(k0 >> 11), (int)g0, &full[slot]);
-                            tma3d(st + a.rs * klen, &a.tm1, 0, (int)(k0 >> 11), (int)g0, &full[slot]);
+                            tma3d(st, &a.tm0, 0, (int)(k0 >> 11), (int)g0, &full[slot], pol_w);
+                            tma3d(st + a.rs * klen, &a.tm1, 0, (int)(k0 >> 11), (int)g0, &full[slot], pol_w);
                         }
                     }
                 }
@@ -333,13 +368,13 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             for (int r = whole ? 32 : lane; r < nr; r += 32) {
                 const uint64_t off = (uint64_t)(g0 + r) * K + k0;
                 if (FMT == FMT_PAL) {
-                    bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
-                    bulk_g2s(st + a.rs * klen + r * (klen / 2), a.w.codes + off / 2, klen / 2, &full[slot]);
+                    bulk_g2s_hint(st + r * klen, a.w.sm + off, klen, &full[slot], pol_w);
+                    bulk_g2s_hint(st + a.rs * klen + r * (klen / 2), a.w.codes + off / 2, klen / 2, &full[slot], pol_w);
                 } else if (FMT == FMT_EXP) {
-                    bulk_g2s(st + r * klen, a.w.sm + off, klen, &full[slot]);
-                    bulk_g2s(st + a.rs * klen + r * klen, a.w.exps + off, klen, &full[slot]);
+                    bulk_g2s_hint(st + r * klen, a.w.sm + off, klen, &full[slot], pol_w);
+                    bulk_g2s_hint(st + a.rs * klen + r * klen, a.w.exps + off, klen, &full[slot], pol_w);
                 } else {
-                    bulk_g2s(st + r * 2 * klen, a.w.w + off, 2 * klen, &full[slot]);
+                    bulk_g2s_hint(st + r * 2 * klen, a.w.w + off, 2 * klen, &full[slot], pol_w);
                 }
             }
             issued = i + 1;
@@ -388,8 +423,8 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
             if (kk < klen && b0 + j < a.B) {
                 const uint4 *src = (const uint4 *)(a.x + (b0 + j) * K + k0 + kk);
-                lo = __ldg(src);
-                hi = __ldg(src + 1);
+                lo = ldg_hint(src, l2_evict_last());
+                hi = ldg_hint(src + 1, l2_evict_last());
             }
 #pragma unroll
             for (int q = 0; q < 4; q++) {
