@@ -248,7 +248,10 @@ uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev, int64_t B
  *   nothing improves), and store the fastest in the matrix's tune table, keyed
  *   by batch bucket.  workspace must hold uw_workspace_size for every candidate
  *   (uw_autotune_workspace_size).  Synchronous.  Writes scratch outputs only
- *   into the workspace.
+ *   into the workspace.  It also allocates, for the duration of the call, a
+ *   device buffer of twice the L2 size that it rewrites before each timed
+ *   launch, so candidates are timed with their weights coming from HBM (if
+ *   that allocation fails, timing proceeds without it).
  */
 uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n_batches, void *workspace, size_t ws_bytes,
                       uw_stream stream);
