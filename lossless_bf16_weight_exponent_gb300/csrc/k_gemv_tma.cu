@@ -21,8 +21,8 @@
 // so a warp's lookups never share a bank.  A stage without verbatim blocks runs a
 // straight-line body; a verbatim block's codes are all zero, so reading a zero table
 // row under a zero sign+mantissa mask makes it add exactly +0 * x, and after the main
-// loop the consumers add the CTA's verbatim blocks' true products (their exponents,
-// sign+mantissa bytes and X from global memory) - no warp runs a slower body that
+// loop the consumers add the CTA's verbatim blocks' true products from records staged
+// in shared memory and X written into the freed ring - no warp runs a slower body that
 // would hold the ring back.  Lane sums of four consecutive stages
 // are reduced together (a transposed butterfly), and row sums meet in shared
 // memory and are written once at the end.  Every
@@ -66,6 +66,7 @@ struct TmaArgs {  // 64-byte aligned through its tensor maps
     int rows_cta;    // max rows owned by one CTA
     int bm_words;    // max verbatim-bitmap words of one CTA's rows
     int w_from_prev; // the weight stream is written by the preceding kernel (a preprocess workspace)
+    int vcap;        // verbatim records of the CTA staged in shared memory (beyond: global loads)
     int *status;
 };
 
@@ -116,8 +117,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
-// L2 policies: the weight streams are read once per launch (evict first); X is read again by the verbatim pass at
-// the end of the launch (evict last)
+// L2 policies: the weight streams are read once per launch (evict first); X is read by every CTA (evict last)
 __device__ __forceinline__ uint64_t l2_evict_first()
 {
     uint64_t p;
@@ -139,14 +139,6 @@ __device__ __forceinline__ uint4 ldg_hint(const void *src, uint64_t pol)
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(src), "l"(pol));
     return v;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol)
@@ -255,6 +247,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     uint8_t *tab = smem;                                                      // [TB] pair table
     uint64_t *full = (uint64_t *)(smem + TB);                                 // [stages]
     uint64_t *empty = full + a.stages;                                        // [stages]
+    uint64_t *vfull = empty + a.stages;                                       // staged verbatim records landed
     uint8_t *zrow = smem + TB + 512;                                          // [128] zeros: verbatim groups' table row
     float *part = (float *)(smem + TB + 1024);                                // [rows_cta][NB]
     const int part_bytes = (a.rows_cta * NB * 4 + 1023) / 1024 * 1024;
@@ -262,64 +255,12 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     uint32_t *bm = (uint32_t *)(smem + TB + 1024 + part_bytes);              // [bm_words] bitmap
     uint32_t *pf = (uint32_t *)(smem + TB + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
     uint8_t *ring = smem + TB + 1024 + part_bytes + 2 * bm_bytes;            // 1024-aligned: tensor copies want 128
+    uint8_t *vx = ring + (size_t)a.stages * a.stage_bytes;                    // [vcap][kVerbRec] verbatim records
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = a.rs * a.wk;  // consumer warps
     const int CT = C * 32;
 
-    // Verbatim blocks.  The main loop counts each as exactly zero, so no consumer warp runs a slower body for them
-    // and holds up the ring; this pass, run by the consumers after the main loop, adds their true products into the
-    // row sums.  (Run before the main loop it delays the first stages; run by the producer warp once it has issued
-    // every stage it is one warp doing serial round trips: both measured slower.)  The CTA's verbatim blocks are
-    // ranks [v_begin, v_end) of the verbatim stream; thread `tid` of `nt` takes every nt-th rank (the word holding
-    // a rank by binary search of the prefix counts) and reads the block's bytes and X from global memory.
-    auto verbatim_products = [&](int tid, int nt) {
-        const uint64_t pol_x = l2_evict_last();
-        if (FMT != FMT_PAL || !nrows) return;
-        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64, kpr = (uint64_t)K / 64;
-        const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
-        const uint64_t lw = (lb >> 5) - wb0;
-        const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
-                                                    : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
-        for (uint64_t v = v_begin + tid; v < v_end; v += nt) {
-            int lo = 0, hi = n_bw - 1;  // the last word whose prefix count is <= v
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if ((uint64_t)pf[mid] <= v) lo = mid;
-                else hi = mid - 1;
-            }
-            const int bit = (int)__fns(bm[lo], 0, (int)(v - pf[lo]) + 1);
-            const uint64_t blk = (wb0 + lo) * 32 + (uint32_t)bit;
-            const uint32_t row = (uint32_t)blk / (uint32_t)kpr;  // (blocks of a matrix fit 32 bits)
-            const int64_t kb = (int64_t)((uint32_t)blk - row * (uint32_t)kpr) * 64;
-            if (bit > 31 || kb < k0 || kb >= k0 + klen) continue;  // another K-slice's block
-            float sum[NB];
-#pragma unroll
-            for (int j = 0; j < NB; j++) sum[j] = 0.f;
-#pragma unroll
-            for (int p = 0; p < 4; p++) {
-                const uint4 ev = __ldg((const uint4 *)(a.w.verb_exp + v * 64 + 16 * p));
-                const uint4 sv = __ldg((const uint4 *)(a.w.sm + blk * 64 + 16 * p));
-#pragma unroll
-                for (int j = 0; j < NB; j++) {
-                    if (b0 + j >= a.B) continue;
-                    const uint4 *xp = (const uint4 *)(a.x + (b0 + j) * K + kb + 16 * p);
-                    const uint4 xa = ldg_hint(xp, pol_x), xb = ldg_hint(xp + 1, pol_x);
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        uint32_t p01, p23;
-                        pairs_from_exps(word_of(sv, q), word_of(ev, q), p01, p23);
-                        const uint4 &xv = q < 2 ? xa : xb;
-                        sum[j] = fma2_bf16(p01, word_of(xv, 2 * (q & 1)), sum[j]);
-                        sum[j] = fma2_bf16(p23, word_of(xv, 2 * (q & 1) + 1), sum[j]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; j++)
-                if (b0 + j < a.B) atomicAdd(&part[(row - r0) * NB + j], sum[j]);
-        }
-    };
     if (threadIdx.x == 0) {
         if (a.tmap) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tm0) : "memory");
@@ -329,6 +270,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], C);
         }
+        mbar_init(vfull, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -344,8 +286,29 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         const uint64_t pol_w = l2_evict_first();
         int issued = 0;
         bool ok = true;
+        bool verb_issued = FMT != FMT_PAL;
         for (int i = 0; i < n_stages; i++) {
             const int slot = i % a.stages;
+            if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
+                // the ring is primed: stage the CTA's verbatim records (ranks [v_begin, v_end) of the verbatim
+                // stream, at most vcap of them) for the verbatim pass after the main loop
+                if (lane == 0) {
+                    uint32_t v_staged = 0;
+                    uint64_t v_begin = 0;
+                    if (nrows) {
+                        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
+                        const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
+                        const uint32_t bw0 = __ldg(a.w.bitmap + (fb >> 5)), pw0 = __ldg(a.w.prefix + (fb >> 5));
+                        const uint32_t bw1 = __ldg(a.w.bitmap + lwd), pw1 = __ldg(a.w.prefix + lwd);
+                        v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
+                        const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
+                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+                    }
+                    mbar_arrive_expect_tx(vfull, v_staged * kVerbRec);
+                    if (v_staged) bulk_g2s_hint(vx, a.w.verb_rec + v_begin * kVerbRec, v_staged * kVerbRec, vfull, pol_w);
+                }
+                verb_issued = true;
+            }
             const int64_t g0 = r0 + (int64_t)i * a.rs;
             const int nr = (int)min((int64_t)a.rs, r1 - g0);
             const bool whole = a.tmap && nr == a.rs && klen == a.ks;  // one tensor copy per stream: the whole stage
@@ -380,6 +343,11 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             issued = i + 1;
         }
         if (lane == 0) {
+            if (FMT == FMT_PAL) {
+                if (!verb_issued) mbar_arrive_expect_tx(vfull, 0);  // no stages (or a timeout before priming)
+                // the staged records must land before the CTA may exit
+                if (!mbar_wait(vfull, 0)) ok = false;
+            }
             if (!ok) {
                 atomicExch(a.status, (int)DEV_TIMEOUT);
                 // drain: every issued stage's copies must land before the CTA may exit
@@ -576,7 +544,94 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             }
         }
     }
-    verbatim_products(ctid, CT);
+    // Verbatim blocks.  The main loop counted every verbatim block as exactly zero, so no warp ran a slower body
+    // for them and held up the ring.  Their true products are added now.  Once every consumer is done with the
+    // ring, the warps of the first row slot write X (the CTA's K-slice, from their registers) into it; then one
+    // thread per verbatim block reads the block's record (exponents, sign+mantissa bytes, block index: staged in
+    // shared memory, or from global memory beyond the staged ones) and X from shared memory.
+    const bool x_in_ring = (size_t)a.stages * a.stage_bytes >= (size_t)NB * klen * 2;
+    if (FMT == FMT_PAL) {
+        asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // the ring is free
+        if (x_in_ring && slot_row == 0) {
+#pragma unroll
+            for (int j = 0; j < NB; j++)
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const int kk = kbase + 512 * g;
+                    if (kk >= klen) continue;
+                    uint4 *dst = (uint4 *)(ring + ((size_t)j * klen + kk) * 2);
+                    dst[0] = make_uint4(xr[j][8 * g], xr[j][8 * g + 1], xr[j][8 * g + 2], xr[j][8 * g + 3]);
+                    dst[1] = make_uint4(xr[j][8 * g + 4], xr[j][8 * g + 5], xr[j][8 * g + 6], xr[j][8 * g + 7]);
+                }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // X is in the ring
+        if (nrows && __all_sync(0xFFFFFFFFu, ok)) {
+            const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
+            const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
+            const uint64_t lw = (lb >> 5) - wb0;
+            const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
+                                                        : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
+            const uint32_t v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+            // four threads per block (16 weights each, lanes 4m .. 4m + 3 of a warp); whole warps step together so
+            // the quarter sums can meet by shuffles
+            const uint32_t kpr = (uint32_t)(K / 64);
+            const uint64_t items = 4 * (v_end - v_begin), span = (items + 31) / 32 * 32;
+            bool wok = true;  // warp-uniform: the staged records have landed
+            if ((uint64_t)(ctid - lane) < items && v_staged) wok = mbar_wait(vfull, 0);
+            wok = __all_sync(0xFFFFFFFFu, wok);
+            if (!wok) ok = false;
+            for (uint64_t it = ctid; it < span && wok; it += CT) {
+                const bool has = it < items;
+                const uint64_t v = v_begin + (has ? it >> 2 : 0);
+                const int qd = (int)(it & 3);
+                const uint64_t vl = v - v_begin;
+                const uint8_t *rec = vl < v_staged ? vx + vl * kVerbRec : nullptr;
+                uint32_t blk = 0;
+                if (has) blk = rec ? *(const uint32_t *)(rec + 128) : __ldg((const uint32_t *)(a.w.verb_rec + v * kVerbRec + 128));
+                const uint32_t row = blk / kpr;
+                const int64_t kb = (int64_t)(blk - row * kpr) * 64;
+                const bool live = has && kb >= k0 && kb < k0 + klen;  // else another K-slice's block
+                float s0[NB], s1[NB];
+#pragma unroll
+                for (int j = 0; j < NB; j++) s0[j] = s1[j] = 0.f;
+                if (live) {
+                    const uint4 ev = rec ? *(const uint4 *)(rec + 16 * qd) : __ldg((const uint4 *)(a.w.verb_rec + v * kVerbRec + 16 * qd));
+                    const uint4 sv = rec ? *(const uint4 *)(rec + 64 + 16 * qd)
+                                         : __ldg((const uint4 *)(a.w.verb_rec + v * kVerbRec + 64 + 16 * qd));
+#pragma unroll
+                    for (int j = 0; j < NB; j++) {
+                        if (b0 + j >= a.B) continue;
+                        const int kl = (int)(kb - k0) + 16 * qd;
+                        uint4 xa, xb;
+                        if (x_in_ring) {
+                            const uint4 *xp = (const uint4 *)(ring + ((size_t)j * klen + kl) * 2);
+                            xa = xp[0];
+                            xb = xp[1];
+                        } else {
+                            const uint4 *xp = (const uint4 *)(a.x + (b0 + j) * K + k0 + kl);
+                            xa = __ldg(xp);
+                            xb = __ldg(xp + 1);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            uint32_t p01, p23;
+                            pairs_from_exps(word_of(sv, q), word_of(ev, q), p01, p23);
+                            const uint4 &xv = q < 2 ? xa : xb;
+                            s0[j] = fma2_bf16(p01, word_of(xv, 2 * (q & 1)), s0[j]);
+                            s1[j] = fma2_bf16(p23, word_of(xv, 2 * (q & 1) + 1), s1[j]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NB; j++) {
+                    float t = s0[j] + s1[j];
+                    t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+                    t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
+                    if (live && qd == 0 && b0 + j < a.B) atomicAdd(&part[(row - r0) * NB + j], t);
+                }
+            }
+        }
+    }
     if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
     asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // row sums complete
     // write the CTA's rows
@@ -623,7 +678,7 @@ cudaError_t launch_lw(int fmt, const TmaArgs &a, dim3 grid, int threads, size_t 
 }
 
 struct TmaShape {
-    int nsplit, ks, lw, wk, rs, stages, stage_bytes, rows_cta, bm_words, ctas;
+    int nsplit, ks, lw, wk, rs, stages, stage_bytes, rows_cta, bm_words, vcap, ctas;
     size_t smem;
 };
 
@@ -666,6 +721,9 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
     s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);
     s.smem = fixed + (size_t)s.stages * s.stage_bytes;
+    // verbatim records in the shared memory left over (at most 512)
+    s.vcap = w.fmt == FMT_PAL && w.verb_rec ? (int)std::min<size_t>(512, (smem_cap - s.smem) / kVerbRec) : 0;
+    s.smem += (size_t)s.vcap * kVerbRec;
     return true;
 }
 
@@ -758,6 +816,7 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
     a.rows_cta = s.rows_cta;
     a.bm_words = s.bm_words;
     a.w_from_prev = w.w_from_prev;
+    a.vcap = s.vcap;
     a.status = status;
     a.tmap = make_stage_maps(w, s, a.tm0, a.tm1) ? 1 : 0;
     if (s.nsplit > 1) {

@@ -46,6 +46,7 @@ struct uw_matrix {
     uint8_t *codes = nullptr;  // resident 4-bit codes (may be null for Huffman)
     const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
     const uint8_t *tmv_data = nullptr;
+    const uint8_t *verb_rec = nullptr;
     int device = 0;
     std::mutex mu;
     std::vector<TuneEntry> tune;
@@ -118,6 +119,10 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     const uint64_t o_tmo = tmv ? take(tmv_off.size() * 4 + 16) : 0;
     const uint64_t o_tmm = tmv ? take(tmv_mask.size() * 4 + 16) : 0;
     const uint64_t o_tmd = tmv ? take(tmv_data.size() + 64) : 0;
+    // verbatim records (exponents + sign+mantissa bytes per verbatim block) for the GEMV's verbatim pass
+    std::vector<uint8_t> vrec;
+    build_verbatim_records(h, p, vrec);
+    const uint64_t o_vr = take(vrec.size() + 64);
 
     uw_matrix *m = new (std::nothrow) uw_matrix();
     if (!m) return fail(UW_ERR_NO_MEMORY, "uw_load: host allocation");
@@ -143,6 +148,8 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
                 (!tmv_data.empty() &&
                  (e = cudaMemcpyAsync(d + o_tmd, tmv_data.data(), tmv_data.size(), cudaMemcpyHostToDevice, st)))))
         return fail_free(cuda_fail(e, "uw_load: verbatim stream upload"));
+    if (!vrec.empty() && (e = cudaMemcpyAsync(d + o_vr, vrec.data(), vrec.size(), cudaMemcpyHostToDevice, st)))
+        return fail_free(cuda_fail(e, "uw_load: verbatim record upload"));
     std::vector<uint8_t> table;
     std::vector<uint32_t> mtable;
     if (h.codec == UW_CODEC_HUFFMAN) {
@@ -174,6 +181,7 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     m->tmv_off = tmv ? (const uint32_t *)(d + o_tmo) : nullptr;
     m->tmv_mask = tmv ? (const uint32_t *)(d + o_tmm) : nullptr;
     m->tmv_data = tmv ? d + o_tmd : nullptr;
+    m->verb_rec = d + o_vr;
     if (h.codec == UW_CODEC_HUFFMAN && want_palette_form) {
         if ((e = (cudaError_t)launch_decode_huffman(v, DEC_CODES, m->codes, st)))
             return fail_free(cuda_fail(e, "uw_load: palette transcode"));
@@ -285,6 +293,7 @@ static WOperand operand_shape(const uw_matrix *m, int strategy)
     w.tmv_off = m->tmv_off;
     w.tmv_mask = m->tmv_mask;
     w.tmv_data = m->tmv_data;
+    w.verb_rec = m->verb_rec;
     w.codes = m->codes;
     w.status = m->v.status;
     return w;
