@@ -174,11 +174,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
     const uint64_t b0 = c * (v.chunk / 64);
     const uint64_t b1 = (n / 64 < b0 + v.chunk / 64) ? n / 64 : b0 + v.chunk / 64;
 
+    // 64-bit bit buffer, MSB-aligned; `nxt` is the next stream word, loaded one refill ahead so the load's
+    // latency hides behind the symbols decoded meanwhile
     uint32_t wi = pos0 >> 5;
     const int sh = pos0 & 31;
     uint64_t buf = (((uint64_t)word_at(wi) << 32) | word_at(wi + 1)) << sh;
     int avail = 64 - sh;
     wi += 2;
+    uint32_t nxt = word_at(wi++);
     uint32_t used = 0;
     const uint32_t budget = pos1 - pos0;
     bool bad = false;
@@ -206,45 +209,59 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
 
     for (uint64_t bs = b0; bs < b1 && !bad; bs += kMaxChunkBlocks) {
         const uint64_t be = min(b1, bs + kMaxChunkBlocks);
-        // bit j of nvmask: block bs + j is not verbatim; verbatim blocks are written here directly
-        uint32_t nvmask = 0;
-#pragma unroll
-        for (int j = 0; j < kMaxChunkBlocks; j++) {
-            const uint64_t b = bs + j;
-            if (b >= be) break;
+        const int nb = (int)(be - bs);
+        // verbatim flags of blocks bs .. be - 1 from one 64-bit window of the bitmap
+        const uint64_t wlo = __ldg(v.bitmap + (bs >> 5));
+        const uint64_t whi = ((bs >> 5) + 1) * 32 < v.n_blocks ? __ldg(v.bitmap + (bs >> 5) + 1) : 0ull;
+        const uint32_t vmask = (uint32_t)(((whi << 32) | wlo) >> (bs & 31)) & ((1u << nb) - 1u);
+        // verbatim blocks are written here directly
+        for (uint32_t m = vmask; m; m &= m - 1) {
+            const uint64_t b = bs + (uint64_t)(__ffs(m) - 1);
             const uint32_t bw = __ldg(v.bitmap + (b >> 5));
-            if ((bw >> (b & 31)) & 1u) {
-                const uint4 *ve = (const uint4 *)(v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64);
-                if (OUT == DEC_CODES) {
-                    uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
-                    o[0] = make_uint4(0, 0, 0, 0);
-                    o[1] = make_uint4(0, 0, 0, 0);
-                } else if (OUT == DEC_EXP) {
-                    uint4 *o = (uint4 *)((uint8_t *)out + b * 64);
+            const uint4 *ve = (const uint4 *)(v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64);
+            if (OUT == DEC_CODES) {
+                uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
+                o[0] = make_uint4(0, 0, 0, 0);
+                o[1] = make_uint4(0, 0, 0, 0);
+            } else if (OUT == DEC_EXP) {
+                uint4 *o = (uint4 *)((uint8_t *)out + b * 64);
 #pragma unroll
-                    for (int q = 0; q < 4; q++) o[q] = ve[q];
-                } else {
-                    uint4 *o = (uint4 *)((uint16_t *)out + b * 64);
-                    const uint4 *sp = (const uint4 *)(v.sm + b * 64);
-#pragma unroll
-                    for (int q = 0; q < 4; q++) store_bf16x16(o + 2 * q, sp[q], ve[q]);
-                }
+                for (int q = 0; q < 4; q++) o[q] = ve[q];
             } else {
-                nvmask |= 1u << j;
+                uint4 *o = (uint4 *)((uint16_t *)out + b * 64);
+                const uint4 *sp = (const uint4 *)(v.sm + b * 64);
+#pragma unroll
+                for (int q = 0; q < 4; q++) store_bf16x16(o + 2 * q, sp[q], ve[q]);
             }
         }
-        const int total = 64 * __popc(nvmask);
-        int produced = 0, fill = 0, word = 0;
+        // the non-verbatim blocks of the group take the group's symbols in order, 16 codes per output word
+        uint32_t rem = ~vmask & ((1u << nb) - 1u);
+        const int total = 64 * __popc(rem);
+        int cur = rem ? __ffs(rem) - 1 : 0, q = 0;
+        int produced = 0, fill = 0;
         uint64_t acc = 0;
         auto put = [&](uint64_t bits4, int cnt) {  // bits4 holds exactly cnt codes
             acc |= bits4 << (4 * fill);
             fill += cnt;
             if (fill >= 16) {
-                const uint64_t b = bs + __fns(nvmask, 0, (word >> 2) + 1);  // the (word/4)-th non-verbatim block
-                emit(b, word & 3, acc);
-                word++;
+                emit(bs + (uint64_t)cur, q, acc);
+                if (++q == 4) {
+                    q = 0;
+                    rem &= rem - 1;
+                    cur = rem ? __ffs(rem) - 1 : 0;
+                }
                 fill -= 16;
                 acc = fill ? bits4 >> (4 * (cnt - fill)) : 0;
+            }
+        };
+        auto advance = [&](uint32_t len) {
+            buf <<= len;
+            avail -= (int)len;
+            used += len;
+            if (avail < 32) {
+                buf |= (uint64_t)nxt << (32 - avail);
+                avail += 32;
+                nxt = word_at(wi++);
             }
         };
         if (multi) {
@@ -253,13 +270,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
                 uint32_t len = e & 15u;
                 int cnt = (int)((e >> 4) & 7u);
                 if (len == 0) { bad = true; len = 1; cnt = 1; }
-                buf <<= len;
-                avail -= (int)len;
-                used += len;
-                if (avail < 32) {
-                    buf |= (uint64_t)word_at(wi++) << (32 - avail);
-                    avail += 32;
-                }
+                advance(len);
                 put(e >> 11, cnt);
                 produced += cnt;
             }
@@ -276,13 +287,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
                 sym = e >> 4;
             }
             if (len == 0) { bad = true; len = 1; }
-            buf <<= len;
-            avail -= (int)len;
-            used += len;
-            if (avail < 32) {
-                buf |= (uint64_t)word_at(wi++) << (32 - avail);
-                avail += 32;
-            }
+            advance(len);
             put(sym, 1);
             produced++;
         }
