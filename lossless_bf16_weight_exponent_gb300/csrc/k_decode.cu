@@ -103,7 +103,6 @@ int launch_decode_palette(const DevView &v, int out_kind, void *out, void *strea
 
 // ------------------------------------------------------------------------------ Huffman decode
 constexpr int kDecThreads = 128;        // chunks per CTA
-constexpr int kBitWindowWords = 0;      // staged bit-stream words per CTA (0: read the stream from global memory)
 
 // 16 codes (a u64 of nibbles) -> 16 exponent bytes through the palette
 __device__ __forceinline__ uint4 exps_of_codes(uint64_t codes, const uint8_t *pal)
@@ -140,9 +139,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
     __shared__ uint16_t pal2[256];  // exponent pair of a code byte: pal[b & 15] | pal[b >> 4] << 8
     const bool multi = v.mtab != nullptr;
     const int L = multi ? 12 : (int)v.max_len;
-    const int tab_words = multi ? 4096 : max(4096, (1 << L) / 4);
     uint32_t *mt = dsm;                               // multi-symbol table, or the single-symbol byte table
-    uint32_t *sbits = dsm + tab_words;                // [kBitWindowWords] this CTA's run of the bit stream
     if (multi) {
         const uint4 *src = (const uint4 *)v.mtab;
         for (int i = threadIdx.x; i < 1024; i += blockDim.x) ((uint4 *)mt)[i] = src[i];
@@ -154,21 +151,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
         pal2[i] = (uint16_t)(v.palette[i & 15] | (v.palette[i >> 4] << 8));
     const uint64_t c_first = (uint64_t)blockIdx.x * kDecThreads;
     const uint64_t c_last = min((uint64_t)v.n_chunks, c_first + kDecThreads);
-    const uint32_t w_start = v.chunk_off[c_first] >> 5;
-    const uint32_t w_stop = ((v.chunk_off[c_last] + 31) >> 5) + 4;  // + lookahead words
-    const bool staged = kBitWindowWords > 0 && (w_stop - w_start) <= (uint32_t)kBitWindowWords;
-    if (staged)
-        for (uint32_t i = threadIdx.x; i < w_stop - w_start; i += blockDim.x) sbits[i] = v.bits[w_start + i];
     __syncthreads();
     const uint8_t *dt = (const uint8_t *)mt;
     const uint64_t c = c_first + threadIdx.x;
     if (c >= c_last) return;
-    // next 32-bit word of the stream (absolute word number); a corrupt stream that runs past the staged window
-    // reads zeros there, and the chunk's length check below reports it
-    auto word_at = [&](uint32_t wn) -> uint32_t {
-        if (staged) return wn < w_stop ? sbits[wn - w_start] : 0u;
-        return v.bits[wn];
-    };
+    // next 32-bit word of the stream (absolute word number); a corrupt stream that runs past the stream's end and
+    // its 512-byte guard reads zeros there, and the chunk's length check reports it
+    const uint32_t w_lim = ((v.chunk_off[v.n_chunks] + 31) >> 5) + 120;
+    auto word_at = [&](uint32_t wn) -> uint32_t { return wn < w_lim ? v.bits[wn] : 0u; };
     const uint64_t n = (uint64_t)v.N * (uint64_t)v.K;
     const uint32_t pos0 = v.chunk_off[c], pos1 = v.chunk_off[c + 1];
     const uint64_t b0 = c * (v.chunk / 64);
@@ -302,7 +292,7 @@ int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *strea
     const int threads = kDecThreads;
     const int blocks = (int)((v.n_chunks + threads - 1) / threads);
     const size_t tab_bytes = v.mtab ? 16384 : std::max<size_t>(16384, (size_t)1 << v.max_len);
-    const size_t smem = tab_bytes + (size_t)kBitWindowWords * 4;  // decode table + bit window
+    const size_t smem = tab_bytes;  // decode table
     cudaStream_t st = (cudaStream_t)stream;
     static bool attr_set = false;  // set once, outside any stream capture (uw_load runs these kernels first)
     if (!attr_set) {
