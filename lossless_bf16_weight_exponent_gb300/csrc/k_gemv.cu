@@ -325,6 +325,10 @@ int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int ou
         const int e = launch_gemv_mma(w, x, B, y, out_bf16, split_k, variant, acc_ws, w.status, stream);
         if (e != cudaErrorInvalidValue) return e;  // else: no tensor map for these operands, use the CUDA-core GEMV
     }
+    if (variant == 8 && gemv_rp_supported(w, B)) {
+        const int e = launch_gemv_rp(w, x, B, y, out_bf16, acc_ws, stream);
+        if (e != cudaErrorInvalidValue) return e;  // else: no tensor map for these operands
+    }
     if (variant != 1 && w.K > 0) {
         // the default (variant 0) falls back to the one-CTA-per-SM shape when two CTAs do not fit
         const int v = (variant == 0 || variant > 5) && !gemv_tma_supported(w, B, 0) ? 2 : variant > 5 ? 0 : variant;

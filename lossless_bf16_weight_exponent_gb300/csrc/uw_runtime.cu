@@ -579,7 +579,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
         // tensor-core kernel, on the default strategy
         {
             std::vector<uw_plan> seeds;
-            for (int v = 0; v <= 7; v++) seeds.push_back(uw_plan{best.strategy, UW_KERNEL_GEMV, 0, v});
+            for (int v = 0; v <= 8; v++) seeds.push_back(uw_plan{best.strategy, UW_KERNEL_GEMV, 0, v});
             seeds.push_back(uw_plan{best.strategy, UW_KERNEL_TC, 0, 0});
             for (const uw_plan &p : seeds) {
                 if (memcmp(&p, &best, sizeof p) == 0) continue;
@@ -595,7 +595,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
                 if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_DIRECT_PALETTE; v++) if (strategy_ok(m, v)) values.push_back(v); }
                 else if (coord == 1) values = {UW_KERNEL_GEMV, UW_KERNEL_TC};
                 else if (coord == 2) values = split_candidates(m);
-                else values = {0, 1, 2, 3, 4, 5, 6, 7};
+                else values = {0, 1, 2, 3, 4, 5, 6, 7, 8};
                 for (int v : values) {
                     uw_plan p = best;
                     if (coord == 0) p.strategy = v;

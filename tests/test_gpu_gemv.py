@@ -17,7 +17,7 @@ from uwtest import run_matmul, strategies_for, tol_ok
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = (0, 1, 2, 3, 4, 5, 6, 7)
+VARIANTS = (0, 1, 2, 3, 4, 5, 6, 7, 8)
 
 
 def _case(N, K, scale, p1, f1, seed):
@@ -30,7 +30,7 @@ def _case(N, K, scale, p1, f1, seed):
     (257, 2112, 8.0, 0.0, 1.0),         # palette entries >= 128 (exponents around 130)
     (96, 28672, 0.015, 1e-4, 100.0),    # long K: 128 weights per lane for 8-warp CTAs
 ])
-@pytest.mark.parametrize("B", [1, 2, 5, 16])
+@pytest.mark.parametrize("B", [1, 2, 5, 16, 32])
 def test_gemv_variants(N, K, scale, p1, f1, B):
     w = _case(N, K, scale, p1, f1, seed=N * 31 + K)
     x = synth.fill((B, K), seed=N + K + B)
@@ -72,3 +72,21 @@ def test_mma_gemv_gate_8b_sampled(B, out_dtype):
         y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_GEMV, 0, v), out_dtype)[:, rows]
         ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
         assert ok, (v, worst)
+
+
+@pytest.mark.parametrize("B", [1, 4, 16, 17, 32])
+@pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
+def test_rp_gemv_gate_8b_sampled(B, out_dtype):
+    # the row-parallel tensor-pipe GEMV (variant 8) at full size on sampled rows, from both weight forms:
+    # resident codes (direct palette) and codes transcoded from the Huffman stream into the workspace
+    mat = synth.gate_8b()
+    w = mat.weights()
+    x = mat.activations(B)
+    rng = np.random.default_rng(100 + B)
+    rows = np.unique(np.concatenate([[0, 127, 128, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
+    yref, absum = oracle.matmul(w, x, rows)
+    m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN), want_palette_form=True)
+    for s in (uw.STRAT_DIRECT_PALETTE, uw.STRAT_PALETTE_TRANSCODE):
+        y = run_matmul(m, x, (s, uw.KERNEL_GEMV, 0, 8), out_dtype)[:, rows]
+        ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
+        assert ok, (s, worst)
