@@ -71,6 +71,7 @@ struct RpArgs {
     int *status;
     int64_t N, B;
     int upk;               // units per row block (K / 256)
+    int w_from_prev;       // the codes were written by the preceding kernel (a preprocess workspace)
     int64_t units;
     uint8_t palette[16];
 };
@@ -128,6 +129,20 @@ __device__ __forceinline__ uint4 verbatim_exps(const RpArgs &a, const uint8_t *v
     return __ldg((const uint4 *)(a.tmv_data + ((uint64_t)__ldg(a.tmv_off + u) + rank) * 64 + 16 * t));
 }
 
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Zeroes the fp32 target of the atomic adds.  Launched as a dependent of the preceding kernel, it lets the
+// matmul that follows it start at once (streaming its weights) and zeroes only once the preceding kernel is done.
+__global__ void zero_target_kernel(float4 *p, int64_t n4, float *tail, int n_tail)
+{
+    grid_launch_dependents();
+    grid_dependency_wait();
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (blockIdx.x == 0 && (int)threadIdx.x < n_tail) tail[threadIdx.x] = 0.f;
+}
+
 // NB: batch tiles of 8 rows (B <= 8 NB)
 template <int NB>
 __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_constant__ RpArgs a)
@@ -149,8 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
     const int nu = (int)(u1 - u0);
     const int upk = a.upk;
 
-    fill_pair_table(tab, a.palette, threadIdx.x, blockDim.x);
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 32 * kWarps) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
@@ -158,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // a dependent launch may start its prologue and stream its own weights from here on
+    grid_launch_dependents();
 
     if (warp == kWarps) {
         // -------------------------------------------------------------------------------- producer
@@ -166,8 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
         int kq = (int)(u0 % upk), s = 0, issued = 0;
         uint32_t ph = 0;
         bool ok = true;
+        // the weights (unless a preprocess kernel just wrote them) are not the preceding kernel's: the first
+        // stages' weight copies leave before the wait for it, their X tiles after it
+        if (a.w_from_prev) grid_dependency_wait();
+        const int primed = a.w_from_prev ? 0 : min(nu, kStages);
         for (int c = 0; c < nu; c++) {
             const int64_t u = u0 + c;
+            if (c == primed && primed > 0 && lane == 0) {
+                grid_dependency_wait();
+                int k2 = (int)(u0 % upk);
+                for (int i = 0; i < primed; i++) {
+                    uint8_t *st = ring + i * kStage;
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        tma2d(st + 3 * kBoxBytes + j * kXTile, &a.tm_x, k2 * kUnitK + 64 * j, 0, &full[i]);
+                    if (++k2 == upk) k2 = 0;
+                }
+            }
             if ((c & 31) == 0) {
                 const int64_t ul = u + lane;
                 o0 = ul <= U ? __ldg(a.tmv_off + ul) : 0u;
@@ -187,8 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
                     tma2d(st, &a.tm_sm, kw, row0, &full[s]);
                     tma2d(st + kBoxBytes, &a.tm_sm, kw + 128, row0, &full[s]);
                     tma2d(st + 2 * kBoxBytes, &a.tm_codes, kw / 2, row0, &full[s]);
+                    if (c >= primed) {
 #pragma unroll
-                    for (int j = 0; j < 4; j++) tma2d(st + 3 * kBoxBytes + j * kXTile, &a.tm_x, kw + 64 * j, 0, &full[s]);
+                        for (int j = 0; j < 4; j++)
+                            tma2d(st + 3 * kBoxBytes + j * kXTile, &a.tm_x, kw + 64 * j, 0, &full[s]);
+                    }
                     bulk_copy(saddr(vs), a.tmv_mask + 16 * u, 64u, fb);
                     if (nv) bulk_copy(saddr(vs + 64), a.tmv_data + (uint64_t)start * 64, nv * 64u, fb);
                 }
@@ -197,6 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
             issued = c + 1;
             if (++kq == upk) { kq = 0; tile++; }
             if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+        if (lane == 0 && primed > 0 && nu == primed) {
+            // every unit fit in the first stages: their X tiles still have to leave
+            grid_dependency_wait();
+            int k2 = (int)(u0 % upk);
+            for (int i = 0; i < primed; i++) {
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    tma2d(ring + i * kStage + 3 * kBoxBytes + j * kXTile, &a.tm_x, k2 * kUnitK + 64 * j, 0, &full[i]);
+                if (++k2 == upk) k2 = 0;
+            }
         }
         if (lane == 0 && !ok) {
             atomicExch(a.status, (int)DEV_TIMEOUT);
@@ -221,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
     const uint32_t o_x0 = 3 * kBoxBytes + 2 * hh * kXTile + g * 128 + (((2 * t) ^ g) << 4);
     const uint32_t o_x1 = 3 * kBoxBytes + 2 * hh * kXTile + g * 128 + (((2 * t + 1) ^ g) << 4);
     const int wi_base = rg >> 1, bsh = 16 * (rg & 1);
+    fill_pair_table(tab, a.palette, threadIdx.x, 32 * kWarps);
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * kWarps) : "memory");  // the table, among the consumer warps
+    grid_dependency_wait();  // the target is zeroed by the preceding kernel
 
     float acc[NB][4];
 #pragma unroll
@@ -323,8 +371,33 @@ cudaError_t launch_rp_nb(const RpArgs &a, int grid, cudaStream_t st)
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    gemv_rp_kernel<NB><<<grid, kThreads, smem_of(NB), st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = smem_of(NB);
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_rp_kernel<NB>, a);
+}
+
+cudaError_t launch_zero_target(float *p, int64_t n, cudaStream_t st)
+{
+    const int64_t n4 = n / 4;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n4 + 255) / 256, (int64_t)num_sms()));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256u);
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, zero_target_kernel, (float4 *)p, n4, p + 4 * n4, (int)(n - 4 * n4));
 }
 
 }  // namespace
@@ -362,7 +435,9 @@ int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int
     // zeroed fp32 target
     a.acc = out_bf16 ? acc_ws : (float *)y;
     if (!a.acc) return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(a.acc, 0, (size_t)B * N * 4, st);
+    a.w_from_prev = w.w_from_prev;
+    if ((uintptr_t)a.acc & 15) return cudaErrorInvalidValue;
+    cudaError_t e = launch_zero_target(a.acc, B * w.N, st);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(num_sms(), units);
     switch (nb) {
