@@ -106,7 +106,7 @@ typedef struct {
                               *   6, 7:    GEMV on the tensor pipe (mma.sync, fp32 accumulate), B <= 16,
                               *            K a multiple of 256 (6: K-slices of 4096 weights up to B = 8;
                               *            7: of 2048)
-                              *   8:       GEMV on the tensor pipe, B <= 32, K a multiple of 256: one CTA per
+                              *   8:       GEMV on the tensor pipe, B <= 64, K a multiple of 256: one CTA per
                               *            SM walks an even share of the 128-row x 256-weight units, each warp
                               *            owning 8 rows (split_k ignored)
                               * UW_KERNEL_TC: 0, 1: rebuilt tiles in shared memory; 2: rebuilt weights in tensor

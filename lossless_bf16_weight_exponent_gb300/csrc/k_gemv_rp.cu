@@ -1,5 +1,5 @@
 // k_gemv_rp.cu - fused reconstruct + matrix-vector product on the tensor pipe, row-parallel warps (sm_103a),
-// batch 1..32, direct-palette operands.
+// batch 1..64, direct-palette operands.
 //
 // Cloudflare blog "Unweight", section on the reconstructive matmul: the weights are rebuilt from the
 // exponent data and the sign+mantissa bytes on chip and fed straight into the product.  This is the
@@ -50,16 +50,17 @@ constexpr int kSmemCap = 227 * 1024;
 
 // verbatim blocks of a unit staged with it (beyond: global loads)
 __host__ __device__ constexpr int vc_of(int NB) { return NB == 4 ? 8 : 16; }
+// ring stages: three up to 32 batch rows, two beyond (the X tiles grow with the batch)
+__host__ __device__ constexpr int stages_of(int NB) { return NB <= 4 ? 3 : 2; }
 __host__ __device__ constexpr int vslot_of(int NB) { return 64 + vc_of(NB) * 64; }
 // one stage: two sm boxes, one code box, four X tiles of 8 NB rows (all 1024-byte multiples)
 __host__ __device__ constexpr uint32_t stage_of(int NB) { return 3 * kBoxBytes + 4 * (uint32_t)NB * 1024; }
-constexpr int kStages = 3;
 // dynamic shared memory: alignment slack, table, barriers, verbatim slots, ring
 constexpr size_t smem_of(int NB)
 {
-    return 1024 + kTab + 256 + (size_t)kStages * vslot_of(NB) + (size_t)kStages * stage_of(NB);
+    return 1024 + kTab + 256 + (size_t)stages_of(NB) * (vslot_of(NB) + stage_of(NB));
 }
-static_assert(smem_of(4) <= (size_t)kSmemCap, "shared memory of the widest batch shape");
+static_assert(smem_of(4) <= (size_t)kSmemCap && smem_of(8) <= (size_t)kSmemCap, "shared memory of the batch shapes");
 
 struct RpArgs {
     CUtensorMap tm_sm;     // sm [N, K] u8, box {128, 128}, 128-byte swizzle
@@ -149,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     constexpr uint32_t kStage = stage_of(NB);
+    constexpr int kStages = stages_of(NB);
     constexpr int kVC = vc_of(NB), kVSlot = vslot_of(NB);
     constexpr uint32_t kXTile = (uint32_t)NB * 1024;  // one X tile: 8 NB rows x 128 B
     const uint32_t pad = (1024u - (saddr(smem_raw) & 1023u)) & 1023u;
@@ -354,10 +356,11 @@ bool make_map_rp(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 
 bool rp_shape(const WOperand &w, int64_t B, int *nb, int64_t *units)
 {
-    if (B < 1 || B > 32 || w.fmt != FMT_PAL || w.N <= 0 || w.K <= 0 || w.K % kUnitK) return false;
+    if (B < 1 || B > 64 || w.fmt != FMT_PAL || w.N <= 0 || w.K <= 0 || w.K % kUnitK) return false;
     if (w.N > (int64_t)INT32_MAX - kRows || w.K > (int64_t)INT32_MAX) return false;
     if (!w.tmv_off || !w.tmv_mask || !w.tmv_data || !w.codes || !tensor_map_encoder()) return false;
     *nb = (int)((B + 7) / 8);
+    if (*nb > 4) *nb = *nb <= 6 ? 6 : 8;
     *units = (w.N + kRows - 1) / kRows * (w.K / kUnitK);
     return true;
 }
@@ -444,7 +447,9 @@ int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int
     case 1: e = launch_rp_nb<1>(a, grid, st); break;
     case 2: e = launch_rp_nb<2>(a, grid, st); break;
     case 3: e = launch_rp_nb<3>(a, grid, st); break;
-    default: e = launch_rp_nb<4>(a, grid, st); break;
+    case 4: e = launch_rp_nb<4>(a, grid, st); break;
+    case 6: e = launch_rp_nb<6>(a, grid, st); break;
+    default: e = launch_rp_nb<8>(a, grid, st); break;
     }
     if (e != cudaSuccess) return e;
     if (out_bf16) return launch_finalize(acc_ws, y, B * w.N, 1, stream);

@@ -112,7 +112,7 @@ bool gemv_mma_supported(const WOperand &w, int64_t B, int variant);
 int launch_gemv_mma(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
                     float *acc_ws, int *status, void *stream);
 // GEMV on the tensor pipe with row-parallel warps over balanced 128 x 256 units, one CTA per SM (GEMV variant 8):
-// B <= 32, 4-bit codes, K % 256 == 0; partial sums of a row block are added into a zeroed fp32 target
+// B <= 64, 4-bit codes, K % 256 == 0; partial sums of a row block are added into a zeroed fp32 target
 bool gemv_rp_supported(const WOperand &w, int64_t B);
 int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);

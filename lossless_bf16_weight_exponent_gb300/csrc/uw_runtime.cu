@@ -323,7 +323,7 @@ static uw_plan default_plan(const uw_matrix *m, int64_t B)
     p.strategy = m->codes ? UW_STRAT_DIRECT_PALETTE : UW_STRAT_PALETTE_TRANSCODE;
     p.kernel = UW_KERNEL_AUTO;
     const WOperand w = operand_shape(m, p.strategy);
-    if (B > 2 && B <= 32 && gemv_rp_supported(w, B)) {
+    if (B >= 2 && B <= 64 && gemv_rp_supported(w, B)) {
         // a few batch rows: the row-parallel tensor-pipe GEMV streams the weights once for all of them
         p.kernel = UW_KERNEL_GEMV;
         p.variant = 8;

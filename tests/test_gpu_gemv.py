@@ -30,7 +30,7 @@ def _case(N, K, scale, p1, f1, seed):
     (257, 2112, 8.0, 0.0, 1.0),         # palette entries >= 128 (exponents around 130)
     (96, 28672, 0.015, 1e-4, 100.0),    # long K: 128 weights per lane for 8-warp CTAs
 ])
-@pytest.mark.parametrize("B", [1, 2, 5, 16, 32])
+@pytest.mark.parametrize("B", [1, 2, 5, 16, 32, 64])
 def test_gemv_variants(N, K, scale, p1, f1, B):
     w = _case(N, K, scale, p1, f1, seed=N * 31 + K)
     x = synth.fill((B, K), seed=N + K + B)
@@ -74,7 +74,7 @@ def test_mma_gemv_gate_8b_sampled(B, out_dtype):
         assert ok, (v, worst)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 17, 32])
+@pytest.mark.parametrize("B", [1, 4, 16, 17, 32, 33, 48, 64])
 @pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
 def test_rp_gemv_gate_8b_sampled(B, out_dtype):
     # the row-parallel tensor-pipe GEMV (variant 8) at full size on sampled rows, from both weight forms:
