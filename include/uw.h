@@ -180,7 +180,9 @@ uw_status uw_decode(const uw_matrix *m, uint16_t *w_dev, uw_stream stream);
 
 /*
  * uw_workspace_size - device workspace bytes uw_matmul needs for (m, B,
- *   strategy) (AUTO: the plan AUTO would pick).  0 is a valid answer.
+ *   strategy) (AUTO: the plan AUTO would pick; an explicit strategy: that
+ *   strategy with the kernel and launch shape AUTO would pair with it at this B).
+ *   0 is a valid answer.
  */
 uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strategy strategy, size_t *bytes);
 
@@ -194,6 +196,8 @@ uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strategy strategy,
  *   DIRECT_PALETTE without resident codes), UW_ERR_WORKSPACE, UW_ERR_CORRUPT,
  *   UW_ERR_CUDA.
  */
+/*   AUTO runs the autotuned plan for B's bucket, else the default plan; an explicit
+ *   strategy runs with the default kernel and launch shape for that strategy and B. */
 uw_status uw_matmul(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev, uw_out_dtype out_dtype,
                     uw_strategy strategy, void *workspace, size_t ws_bytes, uw_stream stream);
 

@@ -317,10 +317,11 @@ static uint64_t split_bytes(const uw_matrix *m, int64_t B, const uw_plan &p, int
     return round_up((uint64_t)B * (uint64_t)m->h.N * 4, 256);
 }
 
-static uw_plan default_plan(const uw_matrix *m, int64_t B)
+// the kernel and launch shape for a strategy and batch when no tuned plan exists
+static uw_plan default_plan_for_strategy(const uw_matrix *m, int64_t B, int strategy)
 {
     uw_plan p{};
-    p.strategy = m->codes ? UW_STRAT_DIRECT_PALETTE : UW_STRAT_PALETTE_TRANSCODE;
+    p.strategy = strategy;
     p.kernel = UW_KERNEL_AUTO;
     const WOperand w = operand_shape(m, p.strategy);
     if (B >= 2 && B <= 64 && gemv_rp_supported(w, B)) {
@@ -338,6 +339,11 @@ static uw_plan default_plan(const uw_matrix *m, int64_t B)
     p.kernel = resolve_kernel(m, p, B);
     if (p.kernel == UW_KERNEL_GEMV && gemv_tma_supported(w, B, 4)) p.variant = 4;
     return p;
+}
+
+static uw_plan default_plan(const uw_matrix *m, int64_t B)
+{
+    return default_plan_for_strategy(m, B, m->codes ? UW_STRAT_DIRECT_PALETTE : UW_STRAT_PALETTE_TRANSCODE);
 }
 
 extern "C" uw_status uw_plan_for(const uw_matrix *m, int64_t B, uw_plan *out)
@@ -385,9 +391,13 @@ extern "C" uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strateg
 {
     clear_error();
     if (!m || !bytes) return fail(UW_ERR_INVALID_ARG, "uw_workspace_size: NULL argument");
+    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_DIRECT_PALETTE))
+        return fail(UW_ERR_INVALID_ARG, "uw_workspace_size: strategy %d out of range", (int)strategy);
+    if (strategy != UW_STRAT_AUTO && !strategy_ok(m, strategy))
+        return fail(UW_ERR_UNSUPPORTED, "strategy %d not available for this matrix", (int)strategy);
     uw_plan p;
     if (strategy == UW_STRAT_AUTO) uw_plan_for(m, B, &p);
-    else { p = uw_plan{}; p.strategy = strategy; p.kernel = UW_KERNEL_AUTO; }
+    else p = default_plan_for_strategy(m, std::max<int64_t>(B, 1), strategy);
     return uw_plan_workspace_size(m, B, &p, bytes);
 }
 
@@ -444,9 +454,14 @@ extern "C" uw_status uw_matmul(const uw_matrix *m, const uint16_t *x, int64_t B,
 {
     clear_error();
     if (!m) return fail(UW_ERR_INVALID_ARG, "uw_matmul: NULL matrix");
+    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_DIRECT_PALETTE))
+        return fail(UW_ERR_INVALID_ARG, "uw_matmul: strategy %d out of range", (int)strategy);
+    if (strategy != UW_STRAT_AUTO && !strategy_ok(m, strategy))
+        return fail(UW_ERR_UNSUPPORTED, "strategy %d not available for this matrix (codec %u, palette form %d)",
+                    (int)strategy, m->h.codec, m->codes != nullptr);
     uw_plan p;
     if (strategy == UW_STRAT_AUTO) uw_plan_for(m, B, &p);
-    else { p = uw_plan{}; p.strategy = strategy; p.kernel = UW_KERNEL_AUTO; }
+    else p = default_plan_for_strategy(m, std::max<int64_t>(B, 1), strategy);
     return uw_matmul_plan(m, x, B, y, od, &p, ws, ws_bytes, stream);
 }
 
