@@ -112,7 +112,9 @@ typedef struct {
                               * UW_KERNEL_TC: 0, 1: rebuilt tiles in shared memory; 2: rebuilt weights in tensor
                               *   memory (B <= 256); 3: as 2 in a persistent grid that splits the
                               *   (row tile, 256-weight step) units evenly over the SMs (B <= 256, K a multiple of
-                              *   256, split_k ignored)
+                              *   256, split_k ignored); 4: persistent over the same units with each 64-weight step
+                              *   rebuilt into shared memory (B <= 512, K a multiple of 256, 4-bit codes, split_k
+                              *   ignored)
                               * a shape that does not fit the matrix or B runs the nearest one that does */
 } uw_plan;
 

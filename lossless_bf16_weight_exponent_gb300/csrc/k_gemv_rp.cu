@@ -387,14 +387,17 @@ cudaError_t launch_rp_nb(const RpArgs &a, int grid, cudaStream_t st)
     return cudaLaunchKernelEx(&cfg, gemv_rp_kernel<NB>, a);
 }
 
-cudaError_t launch_zero_target(float *p, int64_t n, cudaStream_t st)
+
+}  // namespace
+
+int launch_zero_target(float *p, int64_t n, void *stream)
 {
     const int64_t n4 = n / 4;
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n4 + 255) / 256, (int64_t)num_sms()));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256u);
-    cfg.stream = st;
+    cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute la[1];
     la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     la[0].val.programmaticStreamSerializationAllowed = 1;
@@ -402,8 +405,6 @@ cudaError_t launch_zero_target(float *p, int64_t n, cudaStream_t st)
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, zero_target_kernel, (float4 *)p, n4, p + 4 * n4, (int)(n - 4 * n4));
 }
-
-}  // namespace
 
 bool gemv_rp_supported(const WOperand &w, int64_t B)
 {
@@ -440,7 +441,7 @@ int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int
     if (!a.acc) return cudaErrorInvalidValue;
     a.w_from_prev = w.w_from_prev;
     if ((uintptr_t)a.acc & 15) return cudaErrorInvalidValue;
-    cudaError_t e = launch_zero_target(a.acc, B * w.N, st);
+    cudaError_t e = (cudaError_t)launch_zero_target(a.acc, B * w.N, st);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(num_sms(), units);
     switch (nb) {

@@ -1,0 +1,471 @@
+// k_tc4.cu - persistent fused reconstruct + tcgen05 GEMM with the rebuilt weights in shared memory (sm_103a),
+// B <= 512, direct-palette operands.
+//
+// Cloudflare blog "Unweight", section on the reconstructive matmul: compressed inputs are staged by the copy
+// engine, rebuilt on chip and consumed by the tensor cores at once, so the bf16 matrix never reaches HBM.
+// One CTA per SM walks a balanced, contiguous range of units (128 rows of W x 256 weights of K, the units of the
+// tile-major verbatim stream), row block by row block with K innermost; a unit is four 64-weight steps.
+//   - warp 16 (one thread; lanes fetch the unit's verbatim mask words) TMA-loads per step the sign+mantissa box
+//     [128 rows x 64 B] and the code box [128 x 32 B] (dense rows), the activation tile X [BN x 64] bf16 with
+//     the 128-byte swizzle, the unit's 64-byte verbatim mask and up to kVCs of the step's verbatim blocks;
+//   - warps 0-15 rebuild each step: thread (row, chunk) turns 8 sign+mantissa bytes and 4 code bytes into 8
+//     bf16 (one pair-table lookup per two weights) and stores them as one 16-byte chunk of the K-major
+//     128-byte-swizzled A tile; a warp's reads cover whole 128-byte lines and its stores one chunk of every
+//     bank group, so neither conflicts;
+//   - warp 17 (one thread) issues per step four tcgen05.mma (M = 128, N = BN <= 256, K = 16; two per K-slice
+//     above 256) from the A tile and the X tile into the tensor-memory accumulator of the current segment (a run
+//     of units of one row block); two accumulator buffers when they fit;
+//   - warps 18-25 write a finished segment: tcgen05.ld, fp32 atomic adds into a target zeroed just before.
+// Every wait is bounded; on expiry the kernel latches DEV_TIMEOUT, drains its copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "dev_async.cuh"
+#include "uw_internal.h"
+
+namespace uw {
+
+namespace {
+
+using namespace dev;
+
+constexpr int kRows = 128;            // rows per unit (the MMA's M)
+constexpr int kUnitK = 256;           // weights of K per unit
+constexpr int kStepK = 64;            // weights of K per step (one 128-byte swizzle row of bf16)
+constexpr int kRebuildWarps = 16;
+constexpr int kProdWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kEpiWarp0 = 18;
+constexpr int kEpiWarps = 8;          // two per tensor-memory lane quarter
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr uint32_t kSmBytes = kRows * 64;      // sign+mantissa box of a step
+constexpr uint32_t kCodeBytes = kRows * 32;    // code box of a step
+constexpr uint32_t kVOff = kSmBytes + kCodeBytes;
+constexpr int kVCs = 8;                        // verbatim blocks of a step staged with it (beyond: global loads)
+constexpr uint32_t kXOff = 13312;              // after the verbatim slot (64 + 8 x 64 bytes), 1024-aligned
+constexpr uint32_t kASlot = kRows * 128;       // a rebuilt A tile [128 x 64] bf16
+constexpr int kTab = 256 * 128;                // pair table: entry b for lane l at 128 b + 4 l
+constexpr size_t kSmemCap = 227 * 1024;
+static_assert(kVOff + 64 + kVCs * 64 <= kXOff, "step stage layout");
+
+struct Tc4Args {
+    CUtensorMap tm_sm;     // sm [N, K] u8, box {64, 128}, dense
+    CUtensorMap tm_codes;  // codes [N, K/2] u8, box {32, 128}, dense
+    CUtensorMap tm_x;      // X [B, K] bf16, box {64, min(BN, 256)}, 128-byte swizzle
+    const uint32_t *tmv_off, *tmv_mask;
+    const uint8_t *tmv_data;
+    float *acc;            // [B, N] fp32, zeroed before the launch
+    int *status;
+    int64_t N, B, units;
+    int upk, BN, SS, SA, nbuf, buf_stride, tmem_cols, w_from_prev;
+    uint32_t stage_bytes;
+    uint8_t palette[16];
+};
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// generic-proxy writes to shared memory made visible to the tensor cores (async proxy)
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// four bf16x2 pairs of 8 weights from 8 sign+mantissa bytes (S0, S1) and 4 code bytes C
+__device__ __forceinline__ uint4 rebuild8(const uint8_t *tab, uint32_t S0, uint32_t S1, uint32_t C)
+{
+    uint32_t p[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const uint32_t Sw = q < 2 ? S0 : S1;
+        const uint32_t b = prmt(C, 0u, 0x4440u | (uint32_t)q);
+        const uint32_t e = *(const uint32_t *)(tab + b * 128u);
+        p[q] = (__byte_perm(Sw, 0u, (q & 1) ? 0x3322u : 0x1100u) & 0x807F807Fu) | e;
+    }
+    return make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+__device__ __forceinline__ uint4 rebuild8_exps(uint32_t S0, uint32_t S1, uint32_t E0, uint32_t E1)
+{
+    uint4 r;
+    pairs_from_exps(S0, E0, r.x, r.y);
+    pairs_from_exps(S1, E1, r.z, r.w);
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant__ Tc4Args a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (saddr(smem_raw) & 1023u)) & 1023u;
+    const int SS = a.SS, SA = a.SA;
+    const uint32_t SB = a.stage_bytes;
+    uint8_t *ring = smem_raw + pad;                  // [SS][SB]: sm box, code box, verbatim slot, X tile
+    uint8_t *aslots = ring + SS * SB;                // [SA][kASlot]: rebuilt A tiles, 128-byte swizzle
+    uint8_t *tab = aslots + SA * kASlot;             // [kTab]
+    uint64_t *full = (uint64_t *)(tab + kTab);       // [4] a step's copies landed
+    uint64_t *empty = full + 4;                      // [4] a step's MMAs completed (X and the W boxes are free)
+    uint64_t *afull = empty + 4;                     // [4] an A tile is rebuilt
+    uint64_t *aempty = afull + 4;                    // [4] an A tile's MMAs completed
+    uint64_t *accfull = aempty + 4;                  // [2] a segment's MMAs completed
+    uint64_t *accempty = accfull + 2;                // [2] a segment's accumulator was read out
+    uint64_t *done = accempty + 2;                   // [1] every MMA of the CTA completed
+    uint32_t *tmem_slot = (uint32_t *)(done + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t U = a.units, G = gridDim.x;
+    const int64_t u0 = U * blockIdx.x / G, u1 = U * (blockIdx.x + 1) / G;
+    const int nu = (int)(u1 - u0);
+    const int nsteps = 4 * nu;
+    const int upk = a.upk;
+    const int XR = a.BN <= 256 ? a.BN : a.BN / 2;  // X rows per MMA (the MMA's N)
+
+    if (threadIdx.x == 32 * kProdWarp) {
+        for (int s = 0; s < SS; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < SA; s++) {
+            mbar_init(&afull[s], kRebuildWarps);
+            mbar_init(&aempty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], kEpiWarps);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                     "r"(a.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // a dependent launch may start its prologue from here on
+    grid_launch_dependents();
+
+    if (warp == kProdWarp) {
+        // ---------------------------------------------------------------------------------------- copies
+        auto issue_x = [&](uint8_t *st, int kx, uint64_t *bar) {
+            tma2d(st + kXOff, &a.tm_x, kx, 0, bar);
+            if (a.BN > 256) tma2d(st + kXOff + (uint32_t)XR * 128, &a.tm_x, kx, XR, bar);
+        };
+        bool ok = true;
+        // the weights (unless a preprocess kernel just wrote them) are not the preceding kernel's: the first
+        // stages' weight copies leave before the wait for it, their X tiles after it
+        if (a.w_from_prev) grid_dependency_wait();
+        const int primed = a.w_from_prev ? 0 : min(nsteps, SS);
+        auto issue_primed_x = [&]() {
+            grid_dependency_wait();
+            for (int i = 0; i < primed; i++) {
+                const int64_t u = u0 + (i >> 2);
+                issue_x(ring + i * SB, (int)(u % upk) * kUnitK + (i & 3) * kStepK, &full[i]);
+            }
+        };
+        int64_t tile = u0 / upk;
+        int kq = (int)(u0 % upk), s = 0, issued = 0;
+        uint32_t ph = 0, mwl = 0, voff = 0;
+        for (int i = 0; i < nsteps; i++) {
+            const int j = i & 3;
+            const int64_t u = u0 + (i >> 2);
+            if (i == primed && primed > 0 && lane == 0) issue_primed_x();
+            if (j == 0) {
+                // the unit's mask words (lane l < 16: word l = [step l / 4][row word l % 4]) and verbatim offset
+                mwl = lane < 16 ? __ldg(a.tmv_mask + 16 * u + lane) : 0u;
+                voff = __ldg(a.tmv_off + u);
+            }
+            const uint32_t pc = __popc(mwl);
+            const uint32_t cnt = __reduce_add_sync(0xFFFFFFFFu, (lane >> 2) == j ? pc : 0u);
+            const uint32_t pre = __reduce_add_sync(0xFFFFFFFFu, (lane >> 2) < j ? pc : 0u);
+            int go = 1;
+            if (lane == 0) {
+                if (i >= SS && !mbar_wait(&empty[s], ph ^ 1u)) go = 0;
+                else {
+                    const uint32_t nv = min(cnt, (uint32_t)kVCs);
+                    uint8_t *st = ring + s * SB;
+                    const int kx = kq * kUnitK + j * kStepK, row0 = (int)(tile * kRows);
+                    const uint32_t fb = saddr(&full[s]);
+                    mbar_expect_tx(&full[s], kSmBytes + kCodeBytes + 64u + 64u * nv + (uint32_t)a.BN * 128u);
+                    tma2d(st, &a.tm_sm, kx, row0, &full[s]);
+                    tma2d(st + kSmBytes, &a.tm_codes, kx / 2, row0, &full[s]);
+                    bulk_copy(saddr(st + kVOff), a.tmv_mask + 16 * u, 64u, fb);
+                    if (nv) bulk_copy(saddr(st + kVOff + 64), a.tmv_data + (uint64_t)(voff + pre) * 64, nv * 64u, fb);
+                    if (i >= primed) issue_x(st, kx, &full[s]);
+                }
+            }
+            if (!__shfl_sync(0xFFFFFFFFu, go, 0)) { ok = false; break; }
+            issued = i + 1;
+            if (j == 3 && ++kq == upk) { kq = 0; tile++; }
+            if (++s == SS) { s = 0; ph ^= 1u; }
+        }
+        // every step fit in the first stages: their X tiles still have to leave
+        if (lane == 0 && primed > 0 && nsteps == primed) issue_primed_x();
+        if (lane == 0 && !ok) {
+            atomicExch(a.status, (int)DEV_TIMEOUT);
+            for (int i = max(0, issued - SS); i < issued; i++) mbar_wait(&full[i % SS], (i / SS) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t id = idesc_bf16(kRows, XR);
+            bool ok = true, first = false;
+            int s = 0, sa = 0, seg = -1, buf = 0;
+            uint32_t ph = 0, pha = 0;
+            int64_t tile = u0 / upk, seg_t = -1;
+            int kq = (int)(u0 % upk);
+            for (int i = 0; i < nsteps; i++) {
+                const int j = i & 3;
+                if (j == 0 && tile != seg_t) {
+                    // a new segment: its accumulator buffer must have been read out
+                    seg++;
+                    buf = seg % a.nbuf;
+                    if (seg >= a.nbuf && !mbar_wait(&accempty[buf], ((seg / a.nbuf) - 1) & 1)) { ok = false; break; }
+                    first = true;
+                    seg_t = tile;
+                }
+                if (!mbar_wait(&afull[sa], pha) || !mbar_wait(&full[s], ph)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_base = saddr(aslots + sa * kASlot);
+                const uint32_t x_base = saddr(ring + s * SB + kXOff);
+                const uint32_t d = tmem + (uint32_t)(buf * a.buf_stride);
+#pragma unroll
+                for (int kk = 0; kk < kStepK / 16; kk++) {
+                    const uint32_t acc_flag = (first && kk == 0) ? 0u : 1u;
+                    const uint64_t ad = smem_desc_sw128(a_base + 32 * kk);
+                    mma_ss(d, ad, smem_desc_sw128(x_base + 32 * kk), id, acc_flag);
+                    if (a.BN > 256) mma_ss(d + (uint32_t)XR, ad, smem_desc_sw128(x_base + (uint32_t)XR * 128 + 32 * kk), id, acc_flag);
+                }
+                first = false;
+                mma_commit(&aempty[sa]);
+                mma_commit(&empty[s]);
+                if (j == 3) {
+                    const bool last_unit = (i >> 2) + 1 == nu;
+                    if (++kq == upk) { kq = 0; tile++; }
+                    if (last_unit || tile != seg_t) mma_commit(&accfull[buf]);
+                }
+                if (++s == SS) { s = 0; ph ^= 1u; }
+                if (++sa == SA) { sa = 0; pha ^= 1u; }
+            }
+            if (!ok) {
+                atomicExch(a.status, (int)DEV_TIMEOUT);
+                // the epilogue still waits for its segments: let it through (the status marks the result)
+                mma_commit(&accfull[0]);
+                mma_commit(&accfull[1]);
+            }
+            // every MMA issued has completed before the accumulators are freed
+            mma_commit(done);
+            if (!mbar_wait(done, 0)) atomicExch(a.status, (int)DEV_TIMEOUT);
+        }
+    } else if (warp < kRebuildWarps) {
+        // ---------------------------------------------------------------------------------------- rebuild
+        fill_pair_table(tab, a.palette, threadIdx.x, 32 * kRebuildWarps);
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * kRebuildWarps) : "memory");
+        const uint8_t *tab_l = tab + 4 * lane;
+        const int c = lane & 7;  // 16-byte chunk (8 weights) of the row
+        bool ok = true;
+        int s = 0, sa = 0;
+        uint32_t ph = 0, pha = 0;
+        for (int i = 0; i < nsteps; i++) {
+            const int j = i & 3;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            if (i >= SA && !mbar_wait(&aempty[sa], pha ^ 1u)) { ok = false; break; }
+            const uint8_t *st = ring + s * SB;
+            uint8_t *at = aslots + sa * kASlot;
+            const uint32_t *mk = (const uint32_t *)(st + kVOff);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int r = 4 * warp + (lane >> 3) + 64 * h;
+                const uint2 Sv = *(const uint2 *)(st + r * 64 + 8 * c);
+                const uint32_t Cv = *(const uint32_t *)(st + kSmBytes + r * 32 + 4 * c);
+                uint4 v = rebuild8(tab_l, Sv.x, Sv.y, Cv);
+                const int wi = 4 * j + (r >> 5);
+                const uint32_t mw = mk[wi];
+                if ((mw >> ((4 * warp + 64 * h) & 31)) & 0xFu) {
+                    // a verbatim block among the warp's four rows (the same word and bits for every lane)
+                    if ((mw >> (r & 31)) & 1u) {
+                        uint32_t rs = __popc(mw & ((1u << (r & 31)) - 1u));
+                        for (int w2 = 4 * j; w2 < wi; w2++) rs += __popc(mk[w2]);
+                        uint2 E;
+                        if (rs < (uint32_t)kVCs) E = *(const uint2 *)(st + kVOff + 64 + rs * 64 + 8 * c);
+                        else {
+                            uint32_t pre = 0;
+                            for (int w2 = 0; w2 < 4 * j; w2++) pre += __popc(mk[w2]);
+                            const int64_t u = u0 + (i >> 2);
+                            E = __ldg((const uint2 *)(a.tmv_data + ((uint64_t)__ldg(a.tmv_off + u) + pre + rs) * 64 + 8 * c));
+                        }
+                        v = rebuild8_exps(Sv.x, Sv.y, E.x, E.y);
+                    }
+                    __syncwarp();
+                }
+                *(uint4 *)(at + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) = v;
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[sa]);
+            if (++s == SS) { s = 0; ph ^= 1u; }
+            if (++sa == SA) { sa = 0; pha ^= 1u; }
+        }
+        if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
+    } else {
+        // ---------------------------------------------------------------------------------------- epilogue
+        grid_dependency_wait();  // the target is zeroed by the preceding kernel
+        const int q = warp & 3, half = (warp - kEpiWarp0) >> 2;
+        const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        int64_t tile = u0 / upk;
+        int kq = (int)(u0 % upk), seg = 0;
+        for (int cu = 0; cu < nu; cu++) {
+            const int64_t t_cur = tile;
+            if (++kq == upk) { kq = 0; tile++; }
+            if (cu + 1 < nu && tile == t_cur) continue;
+            // segment seg (row block t_cur) is complete once its accumulator is
+            const int buf = seg % a.nbuf;
+            const bool got = mbar_wait(&accfull[buf], (seg / a.nbuf) & 1);
+            if (!got) atomicExch(a.status, (int)DEV_TIMEOUT);
+            tc_fence_after();
+            const int64_t row = t_cur * kRows + 32 * q + lane;
+            for (int c0 = 16 * half; c0 < a.B; c0 += 32) {
+                uint32_t v[16];
+                tmem_ld16(tmem + t_lane + (uint32_t)(buf * a.buf_stride + c0), v);
+                tmem_wait_ld();
+                if (got && row < a.N) {
+#pragma unroll
+                    for (int e = 0; e < 16; e++)
+                        if (c0 + e < a.B) atomicAdd(a.acc + (int64_t)(c0 + e) * a.N + row, __uint_as_float(v[e]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[buf]);
+            seg++;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+    }
+}
+
+bool make_map4(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    auto fn = (PFN_cuTensorMapEncodeTiled_v12000)tensor_map_encoder();
+    if (!fn || !base || ((uintptr_t)base & 15)) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Tc4Shape {
+    int BN, SS, SA, nbuf, buf_stride, tmem_cols;
+    uint32_t stage_bytes;
+    int64_t units;
+    size_t smem;
+};
+
+size_t tc4_smem(const Tc4Shape &s) { return 1024 + (size_t)s.SS * s.stage_bytes + (size_t)s.SA * kASlot + kTab + 256; }
+
+bool tc4_shape(const WOperand &w, int64_t B, Tc4Shape &s)
+{
+    if (B < 1 || B > 512 || w.fmt != FMT_PAL || w.N <= 0 || w.K <= 0 || w.K % kUnitK) return false;
+    if (w.N > (int64_t)INT32_MAX - kRows || w.K > (int64_t)INT32_MAX) return false;
+    if (!w.tmv_off || !w.tmv_mask || !w.tmv_data || !w.codes || !tensor_map_encoder()) return false;
+    s.BN = B <= 256 ? (int)((B + 15) / 16 * 16) : (int)((B + 31) / 32 * 32);
+    s.stage_bytes = kXOff + (uint32_t)s.BN * 128;
+    s.SA = s.BN <= 128 ? 4 : s.BN <= 256 ? 3 : 2;
+    s.SS = 4;
+    while (s.SS > 2 && tc4_smem(s) > kSmemCap) s.SS--;
+    if (tc4_smem(s) > kSmemCap) return false;
+    s.nbuf = s.BN <= 256 ? 2 : 1;
+    s.buf_stride = s.BN <= 128 ? 128 : 256;
+    s.tmem_cols = s.BN <= 128 ? 256 : 512;
+    s.units = (w.N + kRows - 1) / kRows * (w.K / kUnitK);
+    s.smem = tc4_smem(s);
+    return true;
+}
+
+}  // namespace
+
+bool tc4_supported(const WOperand &w, int64_t B)
+{
+    Tc4Shape s;
+    return tc4_shape(w, B, s);
+}
+
+int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream)
+{
+    Tc4Shape s;
+    if (!tc4_shape(w, B, s)) return cudaErrorInvalidValue;
+    cudaStream_t st = (cudaStream_t)stream;
+    Tc4Args a;
+    memset(&a, 0, sizeof a);
+    const uint64_t N = (uint64_t)w.N, K = (uint64_t)w.K;
+    const int XR = s.BN <= 256 ? s.BN : s.BN / 2;
+    bool ok = make_map4(&a.tm_sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.sm, K, N, K, 64, kRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map4(&a.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.codes, K / 2, N, K / 2, 32, kRows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) &&
+              make_map4(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, (uint64_t)B, K * 2, 64, (uint32_t)XR,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return cudaErrorInvalidValue;
+    a.tmv_off = w.tmv_off;
+    a.tmv_mask = w.tmv_mask;
+    a.tmv_data = w.tmv_data;
+    a.status = w.status;
+    a.N = w.N;
+    a.B = B;
+    a.units = s.units;
+    a.upk = (int)(w.K / kUnitK);
+    a.BN = s.BN;
+    a.SS = s.SS;
+    a.SA = s.SA;
+    a.nbuf = s.nbuf;
+    a.buf_stride = s.buf_stride;
+    a.tmem_cols = s.tmem_cols;
+    a.w_from_prev = w.w_from_prev;
+    a.stage_bytes = s.stage_bytes;
+    memcpy(a.palette, w.palette, 16);
+    // a row block's partial sums may come from two CTAs: both add into a zeroed fp32 target
+    a.acc = out_bf16 ? acc_ws : (float *)y;
+    if (!a.acc || ((uintptr_t)a.acc & 15)) return cudaErrorInvalidValue;
+    cudaError_t e = (cudaError_t)launch_zero_target(a.acc, B * w.N, st);
+    if (e != cudaSuccess) return e;
+    static bool attr = false;
+    if (!attr) {
+        e = cudaFuncSetAttribute(tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>(num_sms(), s.units));
+    cfg.blockDim = dim3((unsigned)kThreads);
+    cfg.dynamicSmemBytes = s.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc4_kernel, a);
+    if (e != cudaSuccess) return e;
+    if (out_bf16) return launch_finalize(acc_ws, y, B * w.N, 1, stream);
+    return cudaSuccess;
+}
+
+}  // namespace uw

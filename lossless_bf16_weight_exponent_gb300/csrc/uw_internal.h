@@ -115,6 +115,13 @@ int launch_gemv_mma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
 // B <= 64, 4-bit codes, K % 256 == 0; partial sums of a row block are added into a zeroed fp32 target
 bool gemv_rp_supported(const WOperand &w, int64_t B);
 int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
+// zeroes the fp32 target of atomic adds (count floats, 16-byte aligned) as a dependent launch: it waits for the
+// preceding kernel before writing and lets the following matmul start at once
+int launch_zero_target(float *p, int64_t count, void *stream);
+// persistent tcgen05 GEMM with rebuilt weights in shared memory (tensor-core variant 4): B <= 512, 4-bit codes,
+// K % 256 == 0
+bool tc4_supported(const WOperand &w, int64_t B);
+int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);

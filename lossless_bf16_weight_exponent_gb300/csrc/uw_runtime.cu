@@ -330,6 +330,12 @@ static uw_plan default_plan_for_strategy(const uw_matrix *m, int64_t B, int stra
         p.variant = 8;
         return p;
     }
+    if (B > 64 && tc4_supported(w, B)) {
+        // a dense contraction: the persistent tcgen05 kernel
+        p.kernel = UW_KERNEL_TC;
+        p.variant = 4;
+        return p;
+    }
     if (B > 2 && B <= 16 && gemv_mma_supported(w, B, 6)) {
         // a few batch rows: the tensor-pipe GEMV streams the weights once for all of them
         p.kernel = UW_KERNEL_GEMV;
@@ -602,6 +608,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
             std::vector<uw_plan> seeds;
             for (int v = 0; v <= 8; v++) seeds.push_back(uw_plan{best.strategy, UW_KERNEL_GEMV, 0, v});
             seeds.push_back(uw_plan{best.strategy, UW_KERNEL_TC, 0, 0});
+            seeds.push_back(uw_plan{best.strategy, UW_KERNEL_TC, 0, 4});
             for (const uw_plan &p : seeds) {
                 if (memcmp(&p, &best, sizeof p) == 0) continue;
                 float us;
