@@ -5,17 +5,20 @@
 // engine, rebuilt on chip and consumed by the tensor cores at once, so the bf16 matrix never reaches HBM.
 // One CTA per SM walks a balanced, contiguous range of units (128 rows of W x 256 weights of K, the units of the
 // tile-major verbatim stream), row block by row block with K innermost; a unit is four 64-weight steps.
-//   - warp 16 (one thread; lanes fetch the unit's verbatim mask words) TMA-loads per step the sign+mantissa box
-//     [128 rows x 64 B] and the code box [128 x 32 B] (dense rows), the activation tile X [BN x 64] bf16 with
-//     the 128-byte swizzle, the unit's 64-byte verbatim mask and up to kVCs of the step's verbatim blocks;
+//   - warp 16 (one thread; lanes prefetch the units' verbatim offsets and mask words) TMA-loads per step the
+//     sign+mantissa box [128 rows x 64 B] and the code box [128 x 32 B] (dense rows), the unit's 64-byte verbatim
+//     mask and up to kVCs of the step's verbatim blocks into a deep ring of weight stages, each freed as soon as
+//     it is rebuilt;
+//   - warp 17 (one thread) TMA-loads the activation tile X [BN x 64] bf16 of each step (128-byte swizzle) into
+//     its own ring, each stage freed when the step's MMAs complete;
 //   - warps 0-15 rebuild each step: thread (row, chunk) turns 8 sign+mantissa bytes and 4 code bytes into 8
 //     bf16 (one pair-table lookup per two weights) and stores them as one 16-byte chunk of the K-major
 //     128-byte-swizzled A tile; a warp's reads cover whole 128-byte lines and its stores one chunk of every
 //     bank group, so neither conflicts;
-//   - warp 17 (one thread) issues per step four tcgen05.mma (M = 128, N = BN <= 256, K = 16; two per K-slice
+//   - warp 18 (one thread) issues per step four tcgen05.mma (M = 128, N = BN <= 256, K = 16; two per K-slice
 //     above 256) from the A tile and the X tile into the tensor-memory accumulator of the current segment (a run
 //     of units of one row block); two accumulator buffers when they fit;
-//   - warps 18-25 write a finished segment: tcgen05.ld, fp32 atomic adds into a target zeroed just before.
+//   - warps 19-26 write a finished segment: tcgen05.ld, fp32 atomic adds into a target zeroed just before.
 // Every wait is bounded; on expiry the kernel latches DEV_TIMEOUT, drains its copies and MMAs and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -39,19 +42,23 @@ constexpr int kUnitK = 256;           // weights of K per unit
 constexpr int kStepK = 64;            // weights of K per step (one 128-byte swizzle row of bf16)
 constexpr int kRebuildWarps = 16;
 constexpr int kProdWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kEpiWarp0 = 18;
+constexpr int kXWarp = 17;
+constexpr int kMmaWarp = 18;
+constexpr int kEpiWarp0 = 19;
 constexpr int kEpiWarps = 8;          // two per tensor-memory lane quarter
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kSmBytes = kRows * 64;      // sign+mantissa box of a step
 constexpr uint32_t kCodeBytes = kRows * 32;    // code box of a step
 constexpr uint32_t kVOff = kSmBytes + kCodeBytes;
 constexpr int kVCs = 8;                        // verbatim blocks of a step staged with it (beyond: global loads)
-constexpr uint32_t kXOff = 13312;              // after the verbatim slot (64 + 8 x 64 bytes), 1024-aligned
+constexpr uint32_t kWStage = 13312;            // sm box, code box, verbatim slot (64 + 8 x 64 bytes); 1024-aligned
 constexpr uint32_t kASlot = kRows * 128;       // a rebuilt A tile [128 x 64] bf16
-constexpr int kTab = 256 * 128;                // pair table: entry b for lane l at 128 b + 4 l
+constexpr int kTab = 256 * 64;                 // pair table, 16 replicas: entry b for lane l at 64 b + 4 (l % 16)
+constexpr int kMaxSW = 8, kMaxSX = 6, kMaxSA = 4;
+constexpr uint32_t kBarBytes = 512;
 constexpr size_t kSmemCap = 227 * 1024;
-static_assert(kVOff + 64 + kVCs * 64 <= kXOff, "step stage layout");
+static_assert(kVOff + 64 + kVCs * 64 <= kWStage, "weight stage layout");
+static_assert((2 * kMaxSW + 2 * kMaxSX + 2 * kMaxSA + 5) * 8 + 4 <= kBarBytes, "barrier region");
 
 struct Tc4Args {
     CUtensorMap tm_sm;     // sm [N, K] u8, box {64, 128}, dense
@@ -62,8 +69,7 @@ struct Tc4Args {
     float *acc;            // [B, N] fp32, zeroed before the launch
     int *status;
     int64_t N, B, units;
-    int upk, BN, SS, SA, nbuf, buf_stride, tmem_cols, w_from_prev;
-    uint32_t stage_bytes;
+    int upk, BN, SW, SX, SA, nbuf, buf_stride, tmem_cols, w_from_prev;
     uint8_t palette[16];
 };
 
@@ -88,7 +94,7 @@ __device__ __forceinline__ uint4 rebuild8(const uint8_t *tab, uint32_t S0, uint3
     for (int q = 0; q < 4; q++) {
         const uint32_t Sw = q < 2 ? S0 : S1;
         const uint32_t b = prmt(C, 0u, 0x4440u | (uint32_t)q);
-        const uint32_t e = *(const uint32_t *)(tab + b * 128u);
+        const uint32_t e = *(const uint32_t *)(tab + b * 64u);
         p[q] = (__byte_perm(Sw, 0u, (q & 1) ? 0x3322u : 0x1100u) & 0x807F807Fu) | e;
     }
     return make_uint4(p[0], p[1], p[2], p[3]);
@@ -102,20 +108,34 @@ __device__ __forceinline__ uint4 rebuild8_exps(uint32_t S0, uint32_t S1, uint32_
     return r;
 }
 
+// pair table with 16 replicas: for a code byte b the exponent fields of the bf16x2 pair, (pal[b >> 4] << 23) |
+// (pal[b & 15] << 7), at byte offset 64 b + 4 r for replica r
+__device__ __forceinline__ void fill_pair_table16(uint8_t *tab, const uint8_t *palette, int tid, int nthreads)
+{
+    for (int i = tid; i < 256 * 4; i += nthreads) {
+        const int b = i >> 2, q = i & 3;
+        const uint32_t v = ((uint32_t)palette[b >> 4] << 23) | ((uint32_t)palette[b & 15] << 7);
+        *(uint4 *)(tab + 64 * b + 16 * q) = make_uint4(v, v, v, v);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant__ Tc4Args a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (saddr(smem_raw) & 1023u)) & 1023u;
-    const int SS = a.SS, SA = a.SA;
-    const uint32_t SB = a.stage_bytes;
-    uint8_t *ring = smem_raw + pad;                  // [SS][SB]: sm box, code box, verbatim slot, X tile
-    uint8_t *aslots = ring + SS * SB;                // [SA][kASlot]: rebuilt A tiles, 128-byte swizzle
+    const int SW = a.SW, SX = a.SX, SA = a.SA;
+    const uint32_t XB = (uint32_t)a.BN * 128;        // one X tile
+    uint8_t *wring = smem_raw + pad;                 // [SW][kWStage]: sm box, code box, verbatim slot
+    uint8_t *xring = wring + SW * kWStage;           // [SX][XB]: X tiles, 128-byte swizzle
+    uint8_t *aslots = xring + SX * XB;               // [SA][kASlot]: rebuilt A tiles, 128-byte swizzle
     uint8_t *tab = aslots + SA * kASlot;             // [kTab]
-    uint64_t *full = (uint64_t *)(tab + kTab);       // [4] a step's copies landed
-    uint64_t *empty = full + 4;                      // [4] a step's MMAs completed (X and the W boxes are free)
-    uint64_t *afull = empty + 4;                     // [4] an A tile is rebuilt
-    uint64_t *aempty = afull + 4;                    // [4] an A tile's MMAs completed
-    uint64_t *accfull = aempty + 4;                  // [2] a segment's MMAs completed
+    uint64_t *wfull = (uint64_t *)(tab + kTab);      // [SW] a step's weight copies landed
+    uint64_t *wempty = wfull + kMaxSW;               // [SW] the step was rebuilt
+    uint64_t *xfull = wempty + kMaxSW;               // [SX] a step's X tile landed
+    uint64_t *xempty = xfull + kMaxSX;               // [SX] the step's MMAs completed
+    uint64_t *afull = xempty + kMaxSX;               // [SA] an A tile is rebuilt
+    uint64_t *aempty = afull + kMaxSA;               // [SA] an A tile's MMAs completed
+    uint64_t *accfull = aempty + kMaxSA;             // [2] a segment's MMAs completed
     uint64_t *accempty = accfull + 2;                // [2] a segment's accumulator was read out
     uint64_t *done = accempty + 2;                   // [1] every MMA of the CTA completed
     uint32_t *tmem_slot = (uint32_t *)(done + 1);
@@ -129,9 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
     const int XR = a.BN <= 256 ? a.BN : a.BN / 2;  // X rows per MMA (the MMA's N)
 
     if (threadIdx.x == 32 * kProdWarp) {
-        for (int s = 0; s < SS; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < SW; s++) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], kRebuildWarps);
+        }
+        for (int s = 0; s < SX; s++) {
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], 1);
         }
         for (int s = 0; s < SA; s++) {
             mbar_init(&afull[s], kRebuildWarps);
@@ -158,72 +182,85 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
     grid_launch_dependents();
 
     if (warp == kProdWarp) {
-        // ---------------------------------------------------------------------------------------- copies
-        auto issue_x = [&](uint8_t *st, int kx, uint64_t *bar) {
-            tma2d(st + kXOff, &a.tm_x, kx, 0, bar);
-            if (a.BN > 256) tma2d(st + kXOff + (uint32_t)XR * 128, &a.tm_x, kx, XR, bar);
-        };
-        bool ok = true;
-        // the weights (unless a preprocess kernel just wrote them) are not the preceding kernel's: the first
-        // stages' weight copies leave before the wait for it, their X tiles after it
+        // ---------------------------------------------------------------------------------------- weight copies
+        // the weights are not the preceding kernel's unless a preprocess kernel just wrote them
         if (a.w_from_prev) grid_dependency_wait();
-        const int primed = a.w_from_prev ? 0 : min(nsteps, SS);
-        auto issue_primed_x = [&]() {
-            grid_dependency_wait();
-            for (int i = 0; i < primed; i++) {
-                const int64_t u = u0 + (i >> 2);
-                issue_x(ring + i * SB, (int)(u % upk) * kUnitK + (i & 3) * kStepK, &full[i]);
-            }
-        };
+        bool ok = true;
         int64_t tile = u0 / upk;
         int kq = (int)(u0 % upk), s = 0, issued = 0;
-        uint32_t ph = 0, mwl = 0, voff = 0;
+        uint32_t ph = 0, o0 = 0;
+        // lane l < 16: word l of the unit's verbatim mask ([step l / 4][row word l % 4]); the next unit's in flight
+        uint32_t mw_cur = lane < 16 ? __ldg(a.tmv_mask + 16 * u0 + lane) : 0u;
+        uint32_t mw_nxt = (lane < 16 && nu > 1) ? __ldg(a.tmv_mask + 16 * (u0 + 1) + lane) : 0u;
         for (int i = 0; i < nsteps; i++) {
-            const int j = i & 3;
-            const int64_t u = u0 + (i >> 2);
-            if (i == primed && primed > 0 && lane == 0) issue_primed_x();
+            const int j = i & 3, c = i >> 2;
+            const int64_t u = u0 + c;
             if (j == 0) {
-                // the unit's mask words (lane l < 16: word l = [step l / 4][row word l % 4]) and verbatim offset
-                mwl = lane < 16 ? __ldg(a.tmv_mask + 16 * u + lane) : 0u;
-                voff = __ldg(a.tmv_off + u);
+                if ((c & 31) == 0) o0 = u + lane < U ? __ldg(a.tmv_off + u + lane) : 0u;  // 32 units' offsets
+                if (c > 0) {
+                    mw_cur = mw_nxt;
+                    mw_nxt = (lane < 16 && c + 1 < nu) ? __ldg(a.tmv_mask + 16 * (u + 1) + lane) : 0u;
+                }
             }
-            const uint32_t pc = __popc(mwl);
+            const uint32_t voff = __shfl_sync(0xFFFFFFFFu, o0, c & 31);
+            const uint32_t pc = __popc(mw_cur);
             const uint32_t cnt = __reduce_add_sync(0xFFFFFFFFu, (lane >> 2) == j ? pc : 0u);
             const uint32_t pre = __reduce_add_sync(0xFFFFFFFFu, (lane >> 2) < j ? pc : 0u);
             int go = 1;
             if (lane == 0) {
-                if (i >= SS && !mbar_wait(&empty[s], ph ^ 1u)) go = 0;
+                if (i >= SW && !mbar_wait(&wempty[s], ph ^ 1u)) go = 0;
                 else {
                     const uint32_t nv = min(cnt, (uint32_t)kVCs);
-                    uint8_t *st = ring + s * SB;
+                    uint8_t *st = wring + s * kWStage;
                     const int kx = kq * kUnitK + j * kStepK, row0 = (int)(tile * kRows);
-                    const uint32_t fb = saddr(&full[s]);
-                    mbar_expect_tx(&full[s], kSmBytes + kCodeBytes + 64u + 64u * nv + (uint32_t)a.BN * 128u);
-                    tma2d(st, &a.tm_sm, kx, row0, &full[s]);
-                    tma2d(st + kSmBytes, &a.tm_codes, kx / 2, row0, &full[s]);
+                    const uint32_t fb = saddr(&wfull[s]);
+                    mbar_expect_tx(&wfull[s], kSmBytes + kCodeBytes + 64u + 64u * nv);
+                    tma2d(st, &a.tm_sm, kx, row0, &wfull[s]);
+                    tma2d(st + kSmBytes, &a.tm_codes, kx / 2, row0, &wfull[s]);
                     bulk_copy(saddr(st + kVOff), a.tmv_mask + 16 * u, 64u, fb);
                     if (nv) bulk_copy(saddr(st + kVOff + 64), a.tmv_data + (uint64_t)(voff + pre) * 64, nv * 64u, fb);
-                    if (i >= primed) issue_x(st, kx, &full[s]);
                 }
             }
             if (!__shfl_sync(0xFFFFFFFFu, go, 0)) { ok = false; break; }
             issued = i + 1;
             if (j == 3 && ++kq == upk) { kq = 0; tile++; }
-            if (++s == SS) { s = 0; ph ^= 1u; }
+            if (++s == SW) { s = 0; ph ^= 1u; }
         }
-        // every step fit in the first stages: their X tiles still have to leave
-        if (lane == 0 && primed > 0 && nsteps == primed) issue_primed_x();
         if (lane == 0 && !ok) {
             atomicExch(a.status, (int)DEV_TIMEOUT);
-            for (int i = max(0, issued - SS); i < issued; i++) mbar_wait(&full[i % SS], (i / SS) & 1);
+            for (int i = max(0, issued - SW); i < issued; i++) mbar_wait(&wfull[i % SW], (i / SW) & 1);
+        }
+    } else if (warp == kXWarp) {
+        // ---------------------------------------------------------------------------------------- X copies
+        if (lane == 0) {
+            grid_dependency_wait();  // X may be the preceding kernel's output
+            bool ok = true;
+            int kq = (int)(u0 % upk), s = 0, issued = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nsteps; i++) {
+                const int j = i & 3;
+                if (i >= SX && !mbar_wait(&xempty[s], ph ^ 1u)) { ok = false; break; }
+                uint8_t *xt = xring + s * XB;
+                const int kx = kq * kUnitK + j * kStepK;
+                mbar_expect_tx(&xfull[s], XB);
+                tma2d(xt, &a.tm_x, kx, 0, &xfull[s]);
+                if (a.BN > 256) tma2d(xt + (uint32_t)XR * 128, &a.tm_x, kx, XR, &xfull[s]);
+                issued = i + 1;
+                if (j == 3 && ++kq == upk) kq = 0;
+                if (++s == SX) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                atomicExch(a.status, (int)DEV_TIMEOUT);
+                for (int i = max(0, issued - SX); i < issued; i++) mbar_wait(&xfull[i % SX], (i / SX) & 1);
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t id = idesc_bf16(kRows, XR);
             bool ok = true, first = false;
-            int s = 0, sa = 0, seg = -1, buf = 0;
-            uint32_t ph = 0, pha = 0;
+            int sx = 0, sa = 0, seg = -1, buf = 0;
+            uint32_t phx = 0, pha = 0;
             int64_t tile = u0 / upk, seg_t = -1;
             int kq = (int)(u0 % upk);
             for (int i = 0; i < nsteps; i++) {
@@ -236,27 +273,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
                     first = true;
                     seg_t = tile;
                 }
-                if (!mbar_wait(&afull[sa], pha) || !mbar_wait(&full[s], ph)) { ok = false; break; }
+                if (!mbar_wait(&afull[sa], pha) || !mbar_wait(&xfull[sx], phx)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t a_base = saddr(aslots + sa * kASlot);
-                const uint32_t x_base = saddr(ring + s * SB + kXOff);
+                const uint32_t x_base = saddr(xring + sx * XB);
                 const uint32_t d = tmem + (uint32_t)(buf * a.buf_stride);
 #pragma unroll
                 for (int kk = 0; kk < kStepK / 16; kk++) {
                     const uint32_t acc_flag = (first && kk == 0) ? 0u : 1u;
                     const uint64_t ad = smem_desc_sw128(a_base + 32 * kk);
                     mma_ss(d, ad, smem_desc_sw128(x_base + 32 * kk), id, acc_flag);
-                    if (a.BN > 256) mma_ss(d + (uint32_t)XR, ad, smem_desc_sw128(x_base + (uint32_t)XR * 128 + 32 * kk), id, acc_flag);
+                    if (a.BN > 256)
+                        mma_ss(d + (uint32_t)XR, ad, smem_desc_sw128(x_base + (uint32_t)XR * 128 + 32 * kk), id, acc_flag);
                 }
                 first = false;
                 mma_commit(&aempty[sa]);
-                mma_commit(&empty[s]);
+                mma_commit(&xempty[sx]);
                 if (j == 3) {
                     const bool last_unit = (i >> 2) + 1 == nu;
                     if (++kq == upk) { kq = 0; tile++; }
                     if (last_unit || tile != seg_t) mma_commit(&accfull[buf]);
                 }
-                if (++s == SS) { s = 0; ph ^= 1u; }
+                if (++sx == SX) { sx = 0; phx ^= 1u; }
                 if (++sa == SA) { sa = 0; pha ^= 1u; }
             }
             if (!ok) {
@@ -271,18 +309,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
         }
     } else if (warp < kRebuildWarps) {
         // ---------------------------------------------------------------------------------------- rebuild
-        fill_pair_table(tab, a.palette, threadIdx.x, 32 * kRebuildWarps);
+        fill_pair_table16(tab, a.palette, threadIdx.x, 32 * kRebuildWarps);
         asm volatile("bar.sync 1, %0;" ::"r"(32 * kRebuildWarps) : "memory");
-        const uint8_t *tab_l = tab + 4 * lane;
+        const uint8_t *tab_l = tab + 4 * (lane & 15);
         const int c = lane & 7;  // 16-byte chunk (8 weights) of the row
         bool ok = true;
         int s = 0, sa = 0;
         uint32_t ph = 0, pha = 0;
         for (int i = 0; i < nsteps; i++) {
             const int j = i & 3;
-            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            if (!mbar_wait(&wfull[s], ph)) { ok = false; break; }
             if (i >= SA && !mbar_wait(&aempty[sa], pha ^ 1u)) { ok = false; break; }
-            const uint8_t *st = ring + s * SB;
+            const uint8_t *st = wring + s * kWStage;
             uint8_t *at = aslots + sa * kASlot;
             const uint32_t *mk = (const uint32_t *)(st + kVOff);
 #pragma unroll
@@ -314,8 +352,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[sa]);
-            if (++s == SS) { s = 0; ph ^= 1u; }
+            if (lane == 0) {
+                mbar_arrive(&wempty[s]);
+                mbar_arrive(&afull[sa]);
+            }
+            if (++s == SW) { s = 0; ph ^= 1u; }
             if (++sa == SA) { sa = 0; pha ^= 1u; }
         }
         if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
@@ -374,13 +415,15 @@ bool make_map4(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
 }
 
 struct Tc4Shape {
-    int BN, SS, SA, nbuf, buf_stride, tmem_cols;
-    uint32_t stage_bytes;
+    int BN, SW, SX, SA, nbuf, buf_stride, tmem_cols;
     int64_t units;
     size_t smem;
 };
 
-size_t tc4_smem(const Tc4Shape &s) { return 1024 + (size_t)s.SS * s.stage_bytes + (size_t)s.SA * kASlot + kTab + 256; }
+size_t tc4_smem(const Tc4Shape &s)
+{
+    return 1024 + (size_t)s.SW * kWStage + (size_t)s.SX * s.BN * 128 + (size_t)s.SA * kASlot + kTab + kBarBytes;
+}
 
 bool tc4_shape(const WOperand &w, int64_t B, Tc4Shape &s)
 {
@@ -388,17 +431,19 @@ bool tc4_shape(const WOperand &w, int64_t B, Tc4Shape &s)
     if (w.N > (int64_t)INT32_MAX - kRows || w.K > (int64_t)INT32_MAX) return false;
     if (!w.tmv_off || !w.tmv_mask || !w.tmv_data || !w.codes || !tensor_map_encoder()) return false;
     s.BN = B <= 256 ? (int)((B + 15) / 16 * 16) : (int)((B + 31) / 32 * 32);
-    s.stage_bytes = kXOff + (uint32_t)s.BN * 128;
-    s.SA = s.BN <= 128 ? 4 : s.BN <= 256 ? 3 : 2;
-    s.SS = 4;
-    while (s.SS > 2 && tc4_smem(s) > kSmemCap) s.SS--;
-    if (tc4_smem(s) > kSmemCap) return false;
+    // A tiles, then X tiles (about 96 KB of them), then as many weight stages as fit
+    s.SA = s.BN <= 128 ? 3 : 2;
+    s.SX = std::max(2, std::min(kMaxSX, 98304 / (s.BN * 128)));
+    s.SW = 0;
+    const size_t base = tc4_smem(s);
+    if (base + 3 * (size_t)kWStage > kSmemCap) return false;
+    s.SW = (int)std::min<size_t>(kMaxSW, (kSmemCap - base) / kWStage);
     s.nbuf = s.BN <= 256 ? 2 : 1;
     s.buf_stride = s.BN <= 128 ? 128 : 256;
     s.tmem_cols = s.BN <= 128 ? 256 : 512;
     s.units = (w.N + kRows - 1) / kRows * (w.K / kUnitK);
     s.smem = tc4_smem(s);
-    return true;
+    return s.smem <= kSmemCap;
 }
 
 }  // namespace
@@ -433,13 +478,13 @@ int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
     a.units = s.units;
     a.upk = (int)(w.K / kUnitK);
     a.BN = s.BN;
-    a.SS = s.SS;
+    a.SW = s.SW;
+    a.SX = s.SX;
     a.SA = s.SA;
     a.nbuf = s.nbuf;
     a.buf_stride = s.buf_stride;
     a.tmem_cols = s.tmem_cols;
     a.w_from_prev = w.w_from_prev;
-    a.stage_bytes = s.stage_bytes;
     memcpy(a.palette, w.palette, 16);
     // a row block's partial sums may come from two CTAs: both add into a zeroed fp32 target
     a.acc = out_bf16 ? acc_ws : (float *)y;
