@@ -40,13 +40,27 @@ MEASURED_TRAFFIC = {("gate_8b", 1, "gemv_tma_kernel"): 91.928320e6,
 def kernel_name(plan, B):
     """The kernel a plan launches (the dominant kernel of a step), as named in ncu launch lists."""
     import lossless_bf16_weight_exponent_gb300 as uw
-    if plan.kernel == uw.KERNEL_TC or (plan.kernel == uw.KERNEL_AUTO and B > 16):
-        return "tc2_kernel" if plan.variant == 2 and B <= 256 else "tc_kernel"
+    if plan.strategy == uw.STRAT_HUFFMAN_DIRECT:
+        return "gemv_huff_kernel"
+    if plan.kernel == uw.KERNEL_TC or (plan.kernel == uw.KERNEL_AUTO and B > 2):
+        return {4: "tc4_kernel", 3: "tc3_kernel", 2: "tc2_kernel"}.get(plan.variant, "tc_kernel")
+    if plan.variant == 8:
+        return "gemv_rp_kernel"
     if plan.variant in (6, 7) and B <= 16:
         return "gemv_mma_kernel"
     if plan.variant == 1 or B > 2:
         return "gemv_kernel"
     return "gemv_tma_kernel"
+
+
+def launches_per_call(plan, B):
+    """Kernels of this library that one uw_matmul of the plan launches (fp32 output): a preprocess kernel for the
+    Huffman-fed pipelines, the zeroing kernel of the kernels that add into a zeroed target, the matmul kernel.
+    (Memset nodes of the K-split kernels are not kernels of this library.)"""
+    import lossless_bf16_weight_exponent_gb300 as uw
+    pre = 1 if plan.strategy in (uw.STRAT_FULL_DECODE, uw.STRAT_EXP_ONLY, uw.STRAT_PALETTE_TRANSCODE) else 0
+    zero = 1 if kernel_name(plan, B) in ("gemv_rp_kernel", "tc4_kernel", "gemv_huff_kernel") else 0
+    return pre + zero + 1
 
 
 def parse():
@@ -68,6 +82,9 @@ def parse():
                    help="time every configuration (tiny, 8B gate, 8B MLP stack, heavy tail, 70B gate/down) at each of "
                         "its batch sizes under the autotuned plan; one JSON line per (configuration, B)")
     p.add_argument("--stack-layers", type=int, default=32, help="layers of the 8B MLP stack in --sweep")
+    p.add_argument("--resident", default="palette", choices=["palette", "huffman"],
+                   help="what stays resident: the Huffman blob with its palette form (default), or the Huffman blob "
+                        "alone (AUTO then decodes the stream inside the GEMV for B <= 8)")
     return p.parse_args()
 
 
@@ -252,11 +269,12 @@ def run_ours(args):
     mat = workload_matrix(args.workload)
     w = mat.weights()
     blob = uw.encode(w, uw.CODEC_HUFFMAN)
-    base = uw.Matrix(blob, want_palette_form=True)
+    pal_form = args.resident == "palette"
+    base = uw.Matrix(blob, want_palette_form=pal_form)
     info = base.info
     resident = info["device_bytes"]
     copies = max(2, int(np.ceil(3 * L2_BYTES / max(1, resident))))
-    mats = [base] + [uw.Matrix(blob, want_palette_form=True) for _ in range(copies - 1)]
+    mats = [base] + [uw.Matrix(blob, want_palette_form=pal_form) for _ in range(copies - 1)]
 
     # autotune on one copy (batches of the workload), share the table with the others
     tune_batches = [1, 4, 16] if B in (1, 4, 16) else [B]
@@ -338,10 +356,7 @@ def run_ours(args):
     eff_bytes = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
     value = eff_bytes * world * K / (ms_total * 1e-3) / 1e9
 
-    # kernels launched per step by this plan
-    launches_per_step = 1 + (plan.strategy != uw.STRAT_DIRECT_PALETTE)
-    if plan.split_k > 1:
-        launches_per_step += 0  # split accumulation uses a memset node and atomics, no extra kernel for fp32 out
+    launches_per_step = launches_per_call(plan, B)
 
     # e2e through the public API with host buffers: H2D of X and D2H of Y inside the timed region
     xh = torch.from_numpy(mat.activations(B).view(np.int16)).pin_memory()
@@ -359,7 +374,7 @@ def run_ours(args):
     e2e_value = eff_bytes * world * e2e_steps / e2e_s / 1e9
 
     breakdown = {}
-    if not args.no_breakdown and rank == 0 and args.workload == "gate_8b":
+    if not args.no_breakdown and rank == 0 and args.workload == "gate_8b" and pal_form:
         breakdown = strategy_breakdown(mats, mat, info, copies, hbm_peak)
 
     cpu = None
@@ -376,7 +391,8 @@ def run_ours(args):
             "ms_per_step": ms_step, "us_per_matmul": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
             "config": {"workload": f"{args.workload}: W[{mat.N},{mat.K}] bf16 ({mat.name} recipe), "
-                                   f"Huffman blob + resident palette form; X[{B},{mat.K}] N(0,1)",
+                                   + ("Huffman blob + resident palette form" if pal_form else "Huffman blob alone")
+                                   + f"; X[{B},{mat.K}] N(0,1)",
                        "batch": B, "plan": plan.as_tuple(), "copies_rotated": copies,
                        "l2": f"inputs larger than L2: {copies} copies x {resident / 1e6:.1f} MB resident",
                        "compression": {"huffman_bits_per_weight": 8 * info["blob_bytes"] / (mat.N * mat.K),
@@ -408,13 +424,17 @@ def strategy_breakdown(mats, mat, info, copies, hbm_peak):
 
     import lossless_bf16_weight_exponent_gb300 as uw
     out = {}
-    names = {1: "full_decode", 2: "exp_only", 3: "palette_transcode", 4: "direct_palette"}
+    names = {1: "full_decode", 2: "exp_only", 3: "palette_transcode", 4: "direct_palette", 5: "huffman_direct"}
     for B in (1, 4, 16):
         x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
         y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
         eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
         row = {}
         for s, nm in names.items():
+            if s == 5 and B > 8:
+                continue  # the Huffman-direct GEMV takes B <= 8
+            if s == 4 and not mats[0].info["has_palette_form"]:
+                continue
             need = mats[0].workspace_size(B, s)
             ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
             for i in range(6):

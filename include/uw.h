@@ -68,14 +68,27 @@ typedef enum { UW_CODEC_PALETTE = 0, UW_CODEC_HUFFMAN = 1 } uw_codec;
  *   DIRECT_PALETTE     no preprocessing: the fused kernel reads resident 4-bit
  *                      codes (palette codec, or a Huffman matrix loaded with its
  *                      palette form).
- *   AUTO               the autotuned choice for (matrix, B), else a default.
+ *   HUFFMAN_DIRECT     no preprocessing and no palette form: one GEMV kernel
+ *                      decodes the Huffman stream itself (the lookup table in
+ *                      shared memory, as in the post's section on the decode
+ *                      kernels) and multiplies the rebuilt weights straight away.
+ *                      Huffman codec only, code lengths <= 12, chunk_weights a
+ *                      divisor of K of at most 2048, 1 <= B <= 8; runs on
+ *                      UW_KERNEL_GEMV with split_k 0/1 and variant 0 (plain
+ *                      loads) or 1 (each work unit also prefetched into L2 in
+ *                      bulk one unit ahead).  It goes beyond the post's four
+ *                      pipelines.
+ *   AUTO               the autotuned choice for (matrix, B), else a default:
+ *                      DIRECT_PALETTE when the palette form is resident, else
+ *                      HUFFMAN_DIRECT where it applies, else PALETTE_TRANSCODE.
  */
 typedef enum {
     UW_STRAT_AUTO = 0,
     UW_STRAT_FULL_DECODE = 1,
     UW_STRAT_EXP_ONLY = 2,
     UW_STRAT_PALETTE_TRANSCODE = 3,
-    UW_STRAT_DIRECT_PALETTE = 4
+    UW_STRAT_DIRECT_PALETTE = 4,
+    UW_STRAT_HUFFMAN_DIRECT = 5
 } uw_strategy;
 
 typedef enum { UW_OUT_F32 = 0, UW_OUT_BF16 = 1 } uw_out_dtype;

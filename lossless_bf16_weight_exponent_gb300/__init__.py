@@ -23,7 +23,8 @@ OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CORRUPT = 0, 1, 2, 3, 4
 ERR_NO_MEMORY, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_BUFFER_TOO_SMALL = 5, 6, 7, 8, 9
 CODEC_PALETTE, CODEC_HUFFMAN = 0, 1
 STRAT_AUTO, STRAT_FULL_DECODE, STRAT_EXP_ONLY, STRAT_PALETTE_TRANSCODE, STRAT_DIRECT_PALETTE = 0, 1, 2, 3, 4
-STRATEGIES = {"full_decode": 1, "exp_only": 2, "palette_transcode": 3, "direct_palette": 4}
+STRAT_HUFFMAN_DIRECT = 5
+STRATEGIES = {"full_decode": 1, "exp_only": 2, "palette_transcode": 3, "direct_palette": 4, "huffman_direct": 5}
 OUT_F32, OUT_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_TC = 0, 1, 2
 

@@ -115,6 +115,13 @@ int launch_gemv_mma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
 // B <= 64, 4-bit codes, K % 256 == 0; partial sums of a row block are added into a zeroed fp32 target
 bool gemv_rp_supported(const WOperand &w, int64_t B);
 int launch_gemv_rp(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
+// GEMV that decodes the Huffman stream itself (Huffman-direct strategy): B <= 8, a multi-symbol table (code
+// lengths <= 12), chunks of 64..2048 weights (a multiple of 64) that divide K; partial sums of each chunk column
+// are added into a zeroed fp32 target.  Variant 0: plain loads; 1: each unit's rows and stream bytes are also
+// prefetched into L2 in bulk one unit ahead
+bool gemv_huff_supported(const DevView &v, int64_t B, int variant = 0);
+int launch_gemv_huff(const DevView &v, const uint16_t *x, int64_t B, void *y, int out_bf16, int variant, float *acc_ws,
+                     void *stream);
 // zeroes the fp32 target of atomic adds (count floats, 16-byte aligned) as a dependent launch: it waits for the
 // preceding kernel before writing and lets the following matmul start at once
 int launch_zero_target(float *p, int64_t count, void *stream);

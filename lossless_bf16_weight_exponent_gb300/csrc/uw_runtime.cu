@@ -258,6 +258,7 @@ static bool strategy_ok(const uw_matrix *m, int s)
     case UW_STRAT_EXP_ONLY: return true;
     case UW_STRAT_PALETTE_TRANSCODE: return m->h.codec == UW_CODEC_HUFFMAN;
     case UW_STRAT_DIRECT_PALETTE: return m->codes != nullptr;
+    case UW_STRAT_HUFFMAN_DIRECT: return m->h.codec == UW_CODEC_HUFFMAN && gemv_huff_supported(m->v, 1);
     default: return false;
     }
 }
@@ -323,6 +324,11 @@ static uw_plan default_plan_for_strategy(const uw_matrix *m, int64_t B, int stra
     uw_plan p{};
     p.strategy = strategy;
     p.kernel = UW_KERNEL_AUTO;
+    if (strategy == UW_STRAT_HUFFMAN_DIRECT) {
+        // one kernel: the GEMV that decodes the Huffman stream itself
+        p.kernel = UW_KERNEL_GEMV;
+        return p;
+    }
     const WOperand w = operand_shape(m, p.strategy);
     if (B >= 2 && B <= 64 && gemv_rp_supported(w, B)) {
         // a few batch rows: the row-parallel tensor-pipe GEMV streams the weights once for all of them
@@ -349,7 +355,11 @@ static uw_plan default_plan_for_strategy(const uw_matrix *m, int64_t B, int stra
 
 static uw_plan default_plan(const uw_matrix *m, int64_t B)
 {
-    return default_plan_for_strategy(m, B, m->codes ? UW_STRAT_DIRECT_PALETTE : UW_STRAT_PALETTE_TRANSCODE);
+    if (m->codes) return default_plan_for_strategy(m, B, UW_STRAT_DIRECT_PALETTE);
+    // a Huffman matrix without its palette form: decode in the GEMV where it applies, else transcode first
+    if (m->h.codec == UW_CODEC_HUFFMAN && gemv_huff_supported(m->v, B))
+        return default_plan_for_strategy(m, B, UW_STRAT_HUFFMAN_DIRECT);
+    return default_plan_for_strategy(m, B, UW_STRAT_PALETTE_TRANSCODE);
 }
 
 extern "C" uw_status uw_plan_for(const uw_matrix *m, int64_t B, uw_plan *out)
@@ -368,12 +378,22 @@ extern "C" uw_status uw_plan_for(const uw_matrix *m, int64_t B, uw_plan *out)
 
 static uw_status check_plan(const uw_matrix *m, int64_t B, const uw_plan &p, int *kernel)
 {
-    if (p.strategy < UW_STRAT_FULL_DECODE || p.strategy > UW_STRAT_DIRECT_PALETTE)
+    if (p.strategy < UW_STRAT_FULL_DECODE || p.strategy > UW_STRAT_HUFFMAN_DIRECT)
         return fail(UW_ERR_INVALID_ARG, "plan strategy %d out of range", p.strategy);
     if (!strategy_ok(m, p.strategy))
         return fail(UW_ERR_UNSUPPORTED, "strategy %d not available for this matrix (codec %u, palette form %d)", p.strategy,
                     m->h.codec, m->codes != nullptr);
     if (p.split_k < 0 || p.variant < 0) return fail(UW_ERR_INVALID_ARG, "negative split or variant");
+    if (p.strategy == UW_STRAT_HUFFMAN_DIRECT) {
+        if (p.kernel != UW_KERNEL_AUTO && p.kernel != UW_KERNEL_GEMV)
+            return fail(UW_ERR_UNSUPPORTED, "the Huffman-direct strategy runs on the GEMV kernel only");
+        if (p.split_k > 1 || p.variant > 1)
+            return fail(UW_ERR_UNSUPPORTED, "the Huffman-direct GEMV has no K-split and launch variants 0 and 1 only");
+        if (!gemv_huff_supported(m->v, B, p.variant))
+            return fail(UW_ERR_UNSUPPORTED, "the Huffman-direct GEMV takes 1 <= B <= 8 (B=%lld)", (long long)B);
+        *kernel = UW_KERNEL_GEMV;
+        return UW_OK;
+    }
     int k = resolve_kernel(m, p, B);
     if (k == UW_KERNEL_TC && !tc_supported(operand_shape(m, p.strategy), B, p.variant))
         return fail(UW_ERR_UNSUPPORTED, "tensor-core kernel not available for B=%lld variant %d", (long long)B, p.variant);
@@ -397,7 +417,7 @@ extern "C" uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strateg
 {
     clear_error();
     if (!m || !bytes) return fail(UW_ERR_INVALID_ARG, "uw_workspace_size: NULL argument");
-    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_DIRECT_PALETTE))
+    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_HUFFMAN_DIRECT))
         return fail(UW_ERR_INVALID_ARG, "uw_workspace_size: strategy %d out of range", (int)strategy);
     if (strategy != UW_STRAT_AUTO && !strategy_ok(m, strategy))
         return fail(UW_ERR_UNSUPPORTED, "strategy %d not available for this matrix", (int)strategy);
@@ -449,6 +469,11 @@ extern "C" uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x, int64
     }
     if (e) return cuda_fail((cudaError_t)e, "uw_matmul: preprocess launch");
     float *acc = (float *)(wsp + pre);
+    if (plan->strategy == UW_STRAT_HUFFMAN_DIRECT) {
+        e = launch_gemv_huff(m->v, x, B, y, od == UW_OUT_BF16, plan->variant, acc, stream);
+        if (e) return cuda_fail((cudaError_t)e, "uw_matmul: Huffman-direct GEMV launch");
+        return UW_OK;
+    }
     if (kernel == UW_KERNEL_TC) e = launch_tc(w, x, B, y, od == UW_OUT_BF16, plan->split_k, plan->variant, acc, stream);
     else e = launch_gemv(w, x, B, y, od == UW_OUT_BF16, plan->split_k, plan->variant, acc, stream);
     if (e) return cuda_fail((cudaError_t)e, "uw_matmul: matmul launch");
@@ -460,7 +485,7 @@ extern "C" uw_status uw_matmul(const uw_matrix *m, const uint16_t *x, int64_t B,
 {
     clear_error();
     if (!m) return fail(UW_ERR_INVALID_ARG, "uw_matmul: NULL matrix");
-    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_DIRECT_PALETTE))
+    if (strategy != UW_STRAT_AUTO && (strategy < UW_STRAT_FULL_DECODE || strategy > UW_STRAT_HUFFMAN_DIRECT))
         return fail(UW_ERR_INVALID_ARG, "uw_matmul: strategy %d out of range", (int)strategy);
     if (strategy != UW_STRAT_AUTO && !strategy_ok(m, strategy))
         return fail(UW_ERR_UNSUPPORTED, "strategy %d not available for this matrix (codec %u, palette form %d)",
@@ -529,7 +554,7 @@ extern "C" uw_status uw_autotune_workspace_size(const uw_matrix *m, const int64_
     for (int i = 0; i < n; i++) {
         const int64_t B = std::max<int64_t>(batches[i], 1);
         uint64_t pre = 0;
-        for (int s = UW_STRAT_FULL_DECODE; s <= UW_STRAT_DIRECT_PALETTE; s++)
+        for (int s = UW_STRAT_FULL_DECODE; s <= UW_STRAT_HUFFMAN_DIRECT; s++)
             if (strategy_ok(m, s)) pre = std::max(pre, preprocess_bytes(m, s));
         const uint64_t acc = round_up((uint64_t)B * m->h.N * 4, 256);
         const uint64_t xy = round_up((uint64_t)B * m->h.K * 2, 256) + round_up((uint64_t)B * m->h.N * 4, 256);
@@ -620,14 +645,16 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
             bool improved = false;
             for (int coord = 0; coord < 4; coord++) {
                 std::vector<int> values;
-                if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_DIRECT_PALETTE; v++) if (strategy_ok(m, v)) values.push_back(v); }
+                if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_HUFFMAN_DIRECT; v++) if (strategy_ok(m, v)) values.push_back(v); }
                 else if (coord == 1) values = {UW_KERNEL_GEMV, UW_KERNEL_TC};
                 else if (coord == 2) values = split_candidates(m);
                 else values = {0, 1, 2, 3, 4, 5, 6, 7, 8};
                 for (int v : values) {
                     uw_plan p = best;
-                    if (coord == 0) p.strategy = v;
-                    else if (coord == 1) p.kernel = v;
+                    if (coord == 0) {
+                        p.strategy = v;
+                        if (v == UW_STRAT_HUFFMAN_DIRECT) p = default_plan_for_strategy(m, B, v);  // its only shape
+                    } else if (coord == 1) p.kernel = v;
                     else if (coord == 2) p.split_k = v;
                     else p.variant = v;
                     if (memcmp(&p, &best, sizeof p) == 0) continue;
@@ -689,7 +716,7 @@ extern "C" uw_status uw_tune_load(uw_matrix *m, const char *text)
         char extra;
         if (sscanf(line.c_str(), "%lld %d %d %d %d %f %c", &b, &st, &k, &sp, &va, &us, &extra) != 6)
             return fail(UW_ERR_INVALID_ARG, "uw_tune_load: malformed line '%s'", line.c_str());
-        if (b < 1 || (b & (b - 1)) || st < UW_STRAT_FULL_DECODE || st > UW_STRAT_DIRECT_PALETTE || k < UW_KERNEL_GEMV ||
+        if (b < 1 || (b & (b - 1)) || st < UW_STRAT_FULL_DECODE || st > UW_STRAT_HUFFMAN_DIRECT || k < UW_KERNEL_GEMV ||
             k > UW_KERNEL_TC || sp < 0 || va < 0)
             return fail(UW_ERR_INVALID_ARG, "uw_tune_load: out-of-range value in '%s'", line.c_str());
         table.push_back(TuneEntry{b, uw_plan{st, k, sp, va}, us});
