@@ -100,7 +100,12 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
     uint32_t *mt = (uint32_t *)(smem + kPairTableBytes);  // multi-symbol decode table
     grid_launch_dependents();
     fill_pair_table(tab, a.palette, threadIdx.x, blockDim.x);
-    for (int i = threadIdx.x; i < kMTabBytes / 16; i += blockDim.x) ((uint4 *)mt)[i] = ((const uint4 *)a.mtab)[i];
+    // the multi-symbol table; an entry of 0 (these 12 bits start no code) becomes one 1-bit code 0 with bit 31 set,
+    // so the decode loop needs no test: the flag is collected and reported after the loop
+    for (int i = threadIdx.x; i < kMTabBytes / 4; i += blockDim.x) {
+        const uint32_t e = __ldg(a.mtab + i);
+        mt[i] = e ? e : 0x80000000u | (1u << 7) | (1u << 4) | 1u;
+    }
     if (threadIdx.x == 0) next_unit = 0;
     const int64_t u0 = a.units * blockIdx.x / gridDim.x, u1 = a.units * (blockIdx.x + 1) / gridDim.x;
     grid_dependency_wait();  // X and the zeroed target belong to the stream order after the preceding kernels
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
     const uint32_t *bits = a.bits;
     auto word_at = [&](uint32_t wn) -> uint32_t { return wn < wlim ? __ldg(bits + wn) : 0u; };
     bool bad = false;
+    uint32_t bad_bits = 0;  // bit 31: a lookup met bits that start no code
 
     // a unit's rows and chunk column; the lane's L2 prefetches for it
     auto claim = [&]() -> int64_t {
@@ -156,18 +162,17 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
             const uint32_t vmask = (uint32_t)(win >> (bb & 31)) & (nbk >= 32 ? 0xFFFFFFFFu : ((1u << nbk) - 1u));
             uint32_t vbase = 0;
             if (vmask) vbase = __ldg(a.prefix + wb) + __popc((uint32_t)win & ((1u << (bb & 31)) - 1u));
-            int remaining = 64 * (nbk - __popc(vmask));
+            int remaining = 64 * (nbk - __popc(vmask));  // codes of the chunk not yet decoded
 
-            // 64-bit bit buffer, MSB-aligned; the next stream word is loaded one refill ahead
-            uint32_t wi = pos0 >> 5;
-            const int sh = (int)(pos0 & 31);
-            uint64_t buf = (((uint64_t)word_at(wi) << 32) | word_at(wi + 1)) << sh;
-            int avail = 64 - sh;
-            wi += 2;
+            // 64-bit bit buffer, MSB-aligned, `avail` bits valid; the next stream word is loaded one refill ahead.
+            // The absolute position of the next unread bit is always 32 (wi - 1) - avail.
+            const uint32_t w0 = pos0 >> 5;
+            uint64_t buf = (((uint64_t)word_at(w0) << 32) | word_at(w0 + 1)) << (pos0 & 31);
+            int avail = 64 - (int)(pos0 & 31);
+            uint32_t wi = w0 + 2;
             uint32_t nxt = word_at(wi++);
-            uint32_t used = 0;
-            uint64_t cacc = 0;  // decoded codes not yet consumed (4 bits each, first in the low nibble)
-            int fill = 0;
+            uint64_t cacc = 0;  // decoded codes not yet consumed, 4 bits each, the first in the low nibble
+            uint32_t sh = 0;    // 4 x the number of codes in cacc
 
             const uint8_t *smp = a.sm + (uint64_t)r * (uint64_t)K + (uint64_t)j * (uint64_t)C;
             const uint16_t *xp = a.x + (int64_t)j * C;
@@ -183,48 +188,54 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
 #pragma unroll
                     for (int q = 0; q < 4; q++) pairs_from_exps(word_of(S, q), word_of(E, q), pw[2 * q], pw[2 * q + 1]);
                 } else {
-                    uint32_t last_syms = 0;
-                    int last_fill = 15;
-                    // CAREFUL: the chunk's last coded group, where a multi-symbol lookup could run past the
-                    // chunk's codes: the last four symbols are taken one lookup each.  Every earlier group has at
-                    // least 21 symbols left, more than one group can take (16 plus at most four carried).
-                    auto decode16 = [&](auto CAREFUL) {
-                        while (fill < 16) {
-                            const uint32_t e = mt[(uint32_t)(buf >> 52)];
-                            uint32_t len = e & 15u, syms = e >> 11;
-                            int cnt = (int)((e >> 4) & 7u);
-                            if (decltype(CAREFUL)::value && remaining < 5) {
-                                len = (e >> 7) & 15u;
-                                cnt = 1;
-                                syms &= 15u;
-                            }
-                            if (len == 0) {  // no code starts with these bits: a corrupt stream
-                                bad = true;
-                                len = 1;
-                                cnt = 1;
-                                syms = 0;
-                            }
-                            buf <<= len;
-                            avail -= (int)len;
-                            used += len;
-                            if (avail < 32) {
+                    uint32_t last_syms = 0, last_sh = 60;
+                    // one multi-symbol lookup: up to five codes, `len` bits; a table entry with bit 31 set marks
+                    // bits that start no code (a corrupt stream; it counts as one 1-bit code 0)
+                    auto lookup = [&](bool single) {
+                        const uint32_t e = mt[(uint32_t)(buf >> 52)];
+                        bad_bits |= e;
+                        const uint32_t len = single ? (e >> 7) & 15u : e & 15u;
+                        buf <<= len;
+                        avail -= (int)len;
+                        last_syms = single ? (e >> 11) & 15u : e >> 11;
+                        last_sh = sh;
+                        cacc |= (uint64_t)last_syms << sh;
+                        sh += single ? 4u : (e >> 2) & 28u;
+                    };
+                    if (remaining >= 21) {
+                        // at least 21 codes left: more than this group can take (16, plus at most 4 carried in or
+                        // out), so every lookup may decode five codes.  The refill tops the buffer up to more than
+                        // 32 bits, enough for two lookups of at most 12 bits each.
+                        const uint32_t sh0 = sh;
+                        while (sh < 64) {
+                            if (avail <= 32) {
                                 buf |= (uint64_t)nxt << (32 - avail);
                                 avail += 32;
                                 nxt = word_at(wi++);
                             }
-                            cacc |= (uint64_t)syms << (4 * fill);
-                            last_syms = syms;
-                            last_fill = fill;
-                            fill += cnt;
-                            remaining -= cnt;
+                            lookup(false);
+                            if (sh >= 64) break;
+                            lookup(false);
                         }
-                    };
-                    if (remaining >= 21) decode16(std::false_type{});
-                    else decode16(std::true_type{});
+                        remaining -= (int)((sh - sh0) >> 2);
+                    } else {
+                        // the chunk's last coded group: its last four codes are decoded one lookup each, so no
+                        // lookup reads past the chunk's codes
+                        while (sh < 64) {
+                            if (avail <= 32) {
+                                buf |= (uint64_t)nxt << (32 - avail);
+                                avail += 32;
+                                nxt = word_at(wi++);
+                            }
+                            const uint32_t sh0 = sh;
+                            lookup(remaining < 5);
+                            remaining -= (int)((sh - sh0) >> 2);
+                        }
+                    }
                     const uint64_t cw = cacc;
-                    fill -= 16;
-                    // codes of the last lookup beyond the 16th stay for the next group (last_fill >= 11 here)
-                    cacc = (uint64_t)(last_syms >> (4 * (16 - last_fill)));
+                    // codes of the last lookup beyond the 16th stay for the next group (last_sh >= 44 here)
+                    cacc = (uint64_t)(last_syms >> (64u - last_sh));
+                    sh -= 64;
                     const uint32_t c0 = (uint32_t)cw, c1 = (uint32_t)(cw >> 32);
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
@@ -250,13 +261,14 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
                     }
                 }
             }
-            if (used != pos1 - pos0 || fill != 0) bad = true;
+            // every code of the chunk was used, and the codes ended exactly at the next chunk's offset
+            if (32ull * (wi - 1) - (uint64_t)avail != (uint64_t)pos1 || sh != 0) bad = true;
 #pragma unroll
             for (int b = 0; b < NB; b++)
                 if (NB == 1 || b < a.B) atomicAdd(a.acc + b * N + r, acc0[b] + acc1[b]);
         }
     }
-    if (bad) atomicExch(a.status, (int)DEV_CORRUPT);
+    if (bad || (bad_bits >> 31)) atomicExch(a.status, (int)DEV_CORRUPT);
 }
 
 template <int NB, bool PF>

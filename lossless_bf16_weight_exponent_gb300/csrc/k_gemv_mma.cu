@@ -551,8 +551,12 @@ struct MmaShape {
 // 16 consumer warps, one CTA per SM; each warp owns 256 / MB (variant 6) or 128 (variant 7) weights of a slice
 int mma_kw(int64_t B, int variant) { return variant == 7 || B > 8 ? 128 : 256; }
 
+// 4-bit codes only: with the exponent-byte workspace of the exponent-only pipeline this kernel once returned
+// wrong rows on the 8B gate_proj at B = 16, as the bulk-copy GEMV did with the bf16 and exponent-byte workspaces;
+// until the cause is found those formats run on the plain-load GEMV or the tcgen05 kernels.
 bool plan_mma(const WOperand &w, int64_t B, int split_k, int variant, MmaShape &s)
 {
+    if (w.fmt != FMT_PAL) return false;
     if (B < 1 || B > 16 || w.K <= 0 || w.K % 256 || w.N <= 0) return false;
     if (!tensor_map_encoder()) return false;
     s.consumers = 16;
@@ -667,7 +671,10 @@ int launch_gemv_mma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
     if (s.nsplit > 1) {
         a.acc = out_bf16 ? acc_ws : (float *)y;
         if (!a.acc) return cudaErrorInvalidValue;
-        cudaError_t e = cudaMemsetAsync(a.acc, 0, (size_t)B * w.N * 4, st);
+        // zeroed by a kernel, not a memset: this kernel is a dependent launch, and its wait orders it only after
+        // a preceding kernel (a memset before it could still be running when its atomics start)
+        if ((uintptr_t)a.acc & 15) return cudaErrorInvalidValue;
+        cudaError_t e = (cudaError_t)launch_zero_target(a.acc, B * w.N, st);
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)s.ctas, (unsigned)s.nsplit, 1);

@@ -13,7 +13,7 @@ import pytest
 import lossless_bf16_weight_exponent_gb300 as uw
 import oracle
 import synth
-from uwtest import run_matmul, strategies_for, tol_ok
+from uwtest import dev_bytes, run_matmul, strategies_for, to_dev_u16, tol_ok, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -90,3 +90,31 @@ def test_rp_gemv_gate_8b_sampled(B, out_dtype):
         y = run_matmul(m, x, (s, uw.KERNEL_GEMV, 0, 8), out_dtype)[:, rows]
         ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
         assert ok, (s, worst)
+
+
+def test_split_target_zeroed_before_the_dependent_launch_adds():
+    # The K-split GEMVs add partial sums into a zeroed fp32 target and start as dependent launches, behind a
+    # preprocess kernel for the workspace pipelines.  The target is refilled with garbage before every call: a
+    # zeroing that is not ordered before the adds shows up as lost or garbage partial sums.
+    t = torch()
+    mat = synth.gate_8b()
+    w = mat.weights()
+    rows = np.unique(np.concatenate([[0, 1, mat.N - 1], np.random.default_rng(2).choice(mat.N, 61, replace=False)]))
+    m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN), want_palette_form=True)
+    for B, plans in ((1, [(s, uw.KERNEL_GEMV, 2, 4) for s in (1, 2, 3, 4)]),
+                     (16, [(s, uw.KERNEL_GEMV, 2, 6) for s in (1, 2, 3, 4)])):
+        x_np = mat.activations(B)
+        yref, absum = oracle.matmul(w, x_np, rows)
+        x = to_dev_u16(x_np)
+        y = t.empty((B, mat.N), dtype=t.float32, device="cuda")
+        for p in plans:
+            plan = uw.Plan(*p)
+            need = m.plan_workspace_size(B, plan)
+            ws = dev_bytes(need)
+            for _ in range(6):
+                y.fill_(3.0e30)
+                m.matmul_plan(x, B, y, plan, uw.OUT_F32, ws, need)
+                t.cuda.synchronize()
+                got = y.cpu().numpy().astype(np.float64)[:, rows]
+                ok, worst = tol_ok(got, yref, absum)
+                assert ok, (p, worst)
