@@ -514,12 +514,16 @@ def run_sweep(args):
             d.update(extra)
         print(json.dumps(d), flush=True)
 
+    # the same matrices held as the Huffman blob alone (no palette form): the Huffman-fed pipelines
+    single += [("gate_8b/huffman", synth.gate_8b(), [1, 4, 8]), ("gate_70b/huffman", synth.mlp_70b()[0], [1, 8]),
+               ("down_70b/huffman", synth.mlp_70b()[2], [1])]
     for cfg, mat, bs in single:
+        pal_form = not cfg.endswith("/huffman")
         blob = uw.encode(mat.weights(), uw.CODEC_HUFFMAN)
-        base = uw.Matrix(blob, want_palette_form=True)
+        base = uw.Matrix(blob, want_palette_form=pal_form)
         info = base.info
         copies = 1 if cfg == "tiny" else max(2, int(np.ceil(3 * L2_BYTES / info["device_bytes"])))
-        mats = [base] + [uw.Matrix(blob, want_palette_form=True) for _ in range(copies - 1)]
+        mats = [base] + [uw.Matrix(blob, want_palette_form=pal_form) for _ in range(copies - 1)]
         need = base.autotune_workspace_size(bs)
         tws = torch.empty(need, dtype=torch.uint8, device="cuda")
         base.autotune(bs, tws, need)
@@ -536,7 +540,8 @@ def run_sweep(args):
             us = time_graph(lambda i, s: mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s),
                             n, 7, stream) / n
             eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
-            line(cfg, f"W[{mat.N},{mat.K}]", B, us, algorithmic_bytes(info, 4, B), eff, 2.0 * B * mat.N * mat.K,
+            line(cfg, f"W[{mat.N},{mat.K}]", B, us, algorithmic_bytes(info, 4 if pal_form else 5, B), eff,
+                 2.0 * B * mat.N * mat.K,
                  base.plan_for(B).as_tuple(),
                  {"l2": "matrix smaller than L2" if copies == 1 else f"{copies} copies rotated, inputs larger than L2",
                   "verbatim_block_fraction": round(info["n_verbatim"] / info["n_blocks"], 4)})
