@@ -39,9 +39,11 @@ namespace {
 using namespace dev;
 
 // one CTA per SM holds the only copy of the tables, so the SM's unified cache stays mostly L1 (the lanes' row
-// and stream reads are scattered 16- and 4-byte loads that reuse their 32-byte sectors); 32 warps, 24 when each
-// lane keeps eight batch rows of sums
-template <int NB> constexpr int huff_threads() { return NB <= 4 ? 1024 : 768; }
+// and stream reads are scattered 16- and 4-byte loads that reuse their 32-byte sectors); at most 24 warps, so a
+// lane has up to 85 registers
+template <int NB> constexpr int huff_threads() { return 768; }
+// batch rows whose activations are loaded before a group's decode (their latency hides behind it)
+template <int NB> __host__ __device__ constexpr int huff_early_x() { return NB < 2 ? NB : 2; }
 constexpr int kMTabBytes = 4096 * 4;                      // multi-symbol table
 constexpr int kHSmem = kPairTableBytes + kMTabBytes;     // 48 KB
 
@@ -181,6 +183,18 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
             for (int g = 0; g < G; g++) {
                 const uint4 S = S_next;
                 if (g + 1 < G) S_next = ldg_nc16(smp + 16 * (g + 1));
+                constexpr int XE = huff_early_x<NB>();
+                uint4 Xe[XE][2];
+#pragma unroll
+                for (int b = 0; b < XE; b++) {
+                    const uint4 *xs = (const uint4 *)(xp + b * K + 16 * g);
+                    if (NB == 1 || b < a.B) {
+                        Xe[b][0] = __ldg(xs);
+                        Xe[b][1] = __ldg(xs + 1);
+                    } else {
+                        Xe[b][0] = Xe[b][1] = make_uint4(0, 0, 0, 0);
+                    }
+                }
                 uint32_t pw[8];
                 const int blk = g >> 2;
                 if ((vmask >> blk) & 1u) {
@@ -254,7 +268,7 @@ __global__ void __launch_bounds__(huff_threads<NB>(), 1) gemv_huff_kernel(const 
                     const uint4 *xs = (const uint4 *)(xp + b * K + 16 * g);
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
-                        const uint4 X = __ldg(xs + h);
+                        const uint4 X = b < XE ? Xe[b < XE ? b : 0][h] : __ldg(xs + h);
                         acc0[b] = fma2_bf16(pw[4 * h + 0], X.x, acc0[b]);
                         acc1[b] = fma2_bf16(pw[4 * h + 1], X.y, acc1[b]);
                         acc0[b] = fma2_bf16(pw[4 * h + 2], X.z, acc0[b]);
@@ -292,13 +306,13 @@ cudaError_t launch_huff_nb(const HuffArgs &a, int64_t units, cudaStream_t st)
     }
     const int64_t grid = std::min<int64_t>((int64_t)num_sms() * per_sm[dev], units);
     // warps per CTA: a unit is one warp's work and cannot be split, so a CTA's units should fill whole rounds of
-    // its warps (47 units per SM on the 8B gate_proj: 1.97 rounds of 24 warps rather than 1.47 of 32, whose
-    // second round runs half empty).  Among 32, 24 and 16 warps the one with the fullest last round wins; a tie
-    // (within 2%) goes to more warps.
+    // its warps (47 units per SM on the 8B gate_proj: 1.97 rounds of 24 warps; 32 warps would leave the second
+    // of 1.47 rounds half empty).  Of 24 and 16 warps the one with the fuller last round wins; a tie (within 2%)
+    // goes to more warps.
     const int64_t per_cta = (units + grid - 1) / grid;
     int warps = huff_threads<NB>() / 32;
     double best = -1.0;
-    for (int w = huff_threads<NB>() / 32; w >= 16; w -= 8) {
+    for (int w = huff_threads<NB>() / 32; w >= 16; w -= 8) {  // 24 or 16
         const double rounds = (double)per_cta / w, fill = rounds / std::ceil(rounds);
         if (fill > best + 0.02) { best = fill; warps = w; }
     }
