@@ -182,15 +182,20 @@ def gpu_id(dev):
 
 
 def dist_setup():
+    """Rank, world size and local rank from the launcher's environment.  One process per GPU: NCCL when CUDA is
+    present, else gloo (the host-side path the CPU tests run)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return rank, world, local
 
@@ -202,13 +207,21 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The largest of every rank's v (the slowest rank's time bounds the whole job)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_step, steps, world, ms_total):
+    """Whole-job GB/s: every rank runs `steps` steps of `bytes_per_step` (weak scaling: the work per rank is fixed),
+    over the slowest rank's time."""
+    return bytes_per_step * world * steps / (ms_total * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------ CPU oracle (reference arm / baseline)
@@ -354,7 +367,7 @@ def run_ours(args):
     hbm_peak, tf_peak, peak_kind = peaks()
     alg = algorithmic_bytes(info, plan.strategy, B)
     eff_bytes = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
-    value = eff_bytes * world * K / (ms_total * 1e-3) / 1e9
+    value = job_throughput(eff_bytes, K, world, ms_total)
 
     launches_per_step = launches_per_call(plan, B)
 
@@ -371,7 +384,7 @@ def run_ours(args):
     for i in range(e2e_steps):
         mats[i % copies].matmul_host(xh, B, yh, uw.OUT_F32, hws, hneed, stream)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = eff_bytes * world * e2e_steps / e2e_s / 1e9
+    e2e_value = job_throughput(eff_bytes, e2e_steps, world, e2e_s * 1e3)
 
     breakdown = {}
     if not args.no_breakdown and rank == 0 and args.workload == "gate_8b" and pal_form:
