@@ -27,6 +27,33 @@ def test_exports_every_header_symbol():
         assert hasattr(L, s), s
 
 
+def _header_enums():
+    """Every `UW_NAME = value` enumerator of include/uw.h."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(uw.LIB_PATH), "..", "include", "uw.h")).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(UW_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+
+
+def test_binding_constants_match_the_header():
+    # the ctypes binding passes plain integers across the ABI: each of its constants must be the header's value
+    e = _header_enums()
+    pairs = {"UW_STRAT_AUTO": uw.STRAT_AUTO, "UW_STRAT_FULL_DECODE": uw.STRAT_FULL_DECODE,
+             "UW_STRAT_EXP_ONLY": uw.STRAT_EXP_ONLY, "UW_STRAT_PALETTE_TRANSCODE": uw.STRAT_PALETTE_TRANSCODE,
+             "UW_STRAT_DIRECT_PALETTE": uw.STRAT_DIRECT_PALETTE, "UW_STRAT_HUFFMAN_DIRECT": uw.STRAT_HUFFMAN_DIRECT,
+             "UW_CODEC_PALETTE": uw.CODEC_PALETTE, "UW_CODEC_HUFFMAN": uw.CODEC_HUFFMAN,
+             "UW_OUT_F32": uw.OUT_F32, "UW_OUT_BF16": uw.OUT_BF16, "UW_KERNEL_AUTO": uw.KERNEL_AUTO,
+             "UW_KERNEL_GEMV": uw.KERNEL_GEMV, "UW_KERNEL_TC": uw.KERNEL_TC, "UW_OK": uw.OK,
+             "UW_ERR_INVALID_ARG": uw.ERR_INVALID_ARG, "UW_ERR_SHAPE": uw.ERR_SHAPE,
+             "UW_ERR_UNSUPPORTED": uw.ERR_UNSUPPORTED, "UW_ERR_CORRUPT": uw.ERR_CORRUPT,
+             "UW_ERR_NO_MEMORY": uw.ERR_NO_MEMORY, "UW_ERR_WORKSPACE": uw.ERR_WORKSPACE, "UW_ERR_CUDA": uw.ERR_CUDA,
+             "UW_ERR_TIMEOUT": uw.ERR_TIMEOUT, "UW_ERR_BUFFER_TOO_SMALL": uw.ERR_BUFFER_TOO_SMALL}
+    for name, value in pairs.items():
+        assert e.get(name) == value, (name, e.get(name), value)
+    assert sorted(uw.STRATEGIES.values()) == [v for k, v in sorted(e.items(), key=lambda t: t[1])
+                                              if k.startswith("UW_STRAT_") and k != "UW_STRAT_AUTO"]
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(uw, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(uw, "_lib", None)
