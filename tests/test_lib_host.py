@@ -77,7 +77,8 @@ def _cases():
 
 
 @pytest.mark.parametrize("name,w", list(_cases()), ids=[c[0] for c in _cases()])
-@pytest.mark.parametrize("codec,chunk,L", [(0, 256, 12), (1, 256, 12), (1, 64, 4), (1, 192, 15), (1, 1024, 7)])
+@pytest.mark.parametrize("codec,chunk,L", [(0, 256, 12), (1, 256, 12), (1, 64, 4), (1, 192, 15), (1, 1024, 7),
+                                         (1, 2048, 12)])
 def test_encoder_bytes_equal_oracle(name, w, codec, chunk, L):
     a = uw.encode(w, codec, chunk, L)
     b = oracle.encode(w, codec, chunk, L)
