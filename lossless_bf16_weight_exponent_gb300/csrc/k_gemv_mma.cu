@@ -552,8 +552,8 @@ struct MmaShape {
 int mma_kw(int64_t B, int variant) { return variant == 7 || B > 8 ? 128 : 256; }
 
 // 4-bit codes only: with the exponent-byte workspace of the exponent-only pipeline this kernel once returned
-// wrong rows on the 8B gate_proj at B = 16, as the bulk-copy GEMV did with the bf16 and exponent-byte workspaces;
-// until the cause is found those formats run on the plain-load GEMV or the tcgen05 kernels.
+// wrong rows on the 8B gate_proj at B = 16 (K split in two); until the cause is found the workspace formats run on
+// the plain-load GEMV or the tcgen05 kernels.
 bool plan_mma(const WOperand &w, int64_t B, int split_k, int variant, MmaShape &s)
 {
     if (w.fmt != FMT_PAL) return false;

@@ -786,10 +786,10 @@ bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaSha
 
 }  // namespace
 
-// 4-bit codes only.  With the bf16 and exponent-byte workspaces of the full-decode and exponent-only pipelines
-// this kernel intermittently returned a run of wrong rows (about one CTA's range, in one run of four on the 8B
-// gate_proj, with the workspace itself correct afterwards); until the cause is found those formats run on the
-// plain-load GEMV.
+// 4-bit codes only.  With the bf16 workspace of the full-decode pipeline this kernel returned wrong values on a
+// few scattered rows in most runs on the 8B gate_proj (K split in two), with the workspace itself correct
+// afterwards and with kernels serialized as well; the exponent-byte workspace ran clean in the same test.  Until
+// the cause is found, both workspace formats run on the plain-load GEMV.
 bool gemv_tma_supported(const WOperand &w, int64_t B, int variant)
 {
     TmaShape s;
