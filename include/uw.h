@@ -54,8 +54,8 @@ typedef enum {
 typedef enum { UW_CODEC_PALETTE = 0, UW_CODEC_HUFFMAN = 1 } uw_codec;
 
 /*
- * Execution strategies, the four pipelines of the "Unweight" post (section on
- * the four execution pipelines):
+ * Execution strategies: the four pipelines of the "Unweight" post (section on
+ * the four execution pipelines), and a fifth that decodes inside the GEMV:
  *   FULL_DECODE        rebuild the whole BF16 matrix into the workspace, then a
  *                      plain BF16 GEMV/GEMM (the post uses cuBLAS; here a
  *                      hand-written kernel).
