@@ -43,7 +43,7 @@ def kernel_name(plan, B):
     if plan.strategy == uw.STRAT_HUFFMAN_DIRECT:
         return "gemv_huff_kernel"
     if plan.kernel == uw.KERNEL_TC or (plan.kernel == uw.KERNEL_AUTO and B > 2):
-        return {4: "tc4_kernel", 3: "tc3_kernel", 2: "tc2_kernel"}.get(plan.variant, "tc_kernel")
+        return "tc4_kernel" if plan.variant == 4 else "tc_kernel"
     if plan.variant == 8:
         return "gemv_rp_kernel"
     if plan.variant in (6, 7) and B <= 16:

@@ -122,12 +122,10 @@ typedef struct {
                               *   8:       GEMV on the tensor pipe, B <= 64, K a multiple of 256: one CTA per
                               *            SM walks an even share of the 128-row x 256-weight units, each warp
                               *            owning 8 rows (split_k ignored)
-                              * UW_KERNEL_TC: 0, 1: rebuilt tiles in shared memory; 2: rebuilt weights in tensor
-                              *   memory (B <= 256); 3: as 2 in a persistent grid that splits the
-                              *   (row tile, 256-weight step) units evenly over the SMs (B <= 256, K a multiple of
-                              *   256, split_k ignored); 4: persistent over the same units with each 64-weight step
-                              *   rebuilt into shared memory (B <= 512, K a multiple of 256, 4-bit codes, split_k
-                              *   ignored)
+                              * UW_KERNEL_TC: 0, 1: one CTA per 128-row tile and K-slice, rebuilt tiles in shared
+                              *   memory; 4: one CTA per SM over an even share of the 128-row x 256-weight units,
+                              *   each 64-weight step rebuilt into shared memory (B <= 512, K a multiple of 256,
+                              *   4-bit codes, split_k ignored); other values run as 0
                               * a shape that does not fit the matrix or B runs the nearest one that does */
 } uw_plan;
 
@@ -179,7 +177,8 @@ uw_status uw_load(const void *blob, size_t size, int want_palette_form, uw_strea
  */
 uw_status uw_blob_validate(const void *blob, size_t size, uw_info *info);
 
-/* uw_free - release a uw_matrix and its device memory (synchronises the device first). NULL is a no-op. */
+/* uw_free - release a uw_matrix and its device memory.  As with cudaFree (which it calls, and which waits for
+ * work still running on the device), no work that reads the matrix may be enqueued after it.  NULL is a no-op. */
 void uw_free(uw_matrix *m);
 
 /* uw_get_info - header facts and memory footprint of a loaded matrix. */
@@ -249,12 +248,14 @@ uw_status uw_host_workspace_size(const uw_matrix *m, int64_t B, uw_out_dtype out
  *   K-split may need) is a library-owned static device array of 36 MiB, held on
  *   every GPU that loads the library until the process exits.
  *   m must be a Huffman-coded matrix; x_dev, y_dev, B and out_dtype are as in
- *   uw_matmul.  The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call before
- *   any stream capture.  All calls share the one array and it keeps the last
- *   call's contents (the accumulator is cleared on the stream before each use):
- *   calls whose GPU work overlaps (different streams, or different threads
- *   without ordering) race on it.
+ *   uw_matmul.  The array's device address is looked up (cudaGetSymbolAddress)
+ *   by the first call in each CUDA context - the device's primary context, or
+ *   one a driver-API caller made current - and cached under that context's
+ *   unique id, so a call after cudaDeviceReset looks it up again.  Make the
+ *   first call in a context before any stream capture.  All calls share the
+ *   one array and it keeps the last call's contents (the accumulator is
+ *   cleared on the stream before each use): calls whose GPU work overlaps
+ *   (different streams, or different threads without ordering) race on it.
  *   Errors: UW_ERR_WORKSPACE when N*K/2 plus B*N*4 (each rounded up to 256
  *   bytes, with 64 bytes of padding on the codes) exceeds the 36 MiB array;
  *   UW_ERR_UNSUPPORTED for a palette-codec matrix; otherwise as uw_matmul.

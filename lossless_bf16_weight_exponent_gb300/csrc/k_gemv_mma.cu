@@ -98,6 +98,16 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// Hand a ring slot back to the producer once the warp has read it: the slot was read with generic-proxy loads
+// and the next tensor copy writes it through the async proxy, so each lane fences its reads across the proxies
+// (as the PTX memory model requires), the warp converges and one lane arrives on the slot's "empty" barrier.
+__device__ __forceinline__ void release_slot(uint64_t *empty_bar, int lane)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);
+}
+
 // Wait until the barrier's phase with this parity completes; false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
@@ -118,8 +128,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
-// L2 policies: the weight streams are read once per launch (evict first); X is read again by the verbatim pass at
-// the end of the launch (evict last)
+// L2 policies: the weight streams are read once per launch (evict first); X is read by every CTA (evict last)
 __device__ __forceinline__ uint64_t l2_evict_first()
 {
     uint64_t p;
@@ -150,16 +159,6 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int c0,
         "%4}], [%5], %6;" ::"r"(smem_addr(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
-}
-
-// acc += w.lo * x.lo + w.hi * x.hi for bf16x2 w and x, fp32 accumulate
-__device__ __forceinline__ float fma2_bf16(uint32_t w2, uint32_t x2, float acc)
-{
-    asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
-        " fma.rn.f32.bf16 %0, wl, xl, %0;\n fma.rn.f32.bf16 %0, wh, xh, %0;\n}\n"
-        : "+f"(acc)
-        : "r"(w2), "r"(x2));
-    return acc;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
@@ -214,9 +213,10 @@ template <> struct StageFmt<FMT_BF16> { static constexpr int bytes_per_col = 16,
 
 // MB = 1: B <= 8 (A rows g only); MB = 2: B <= 16 (A rows g and g + 8).  KW: weights of the slice per
 // consumer warp (256 keeps K = 4096 in one slice; 128 halves the activation registers)
-// VT: verbatim blocks count as zero in the main loop and their products are added after it (small B); otherwise
-// a verbatim step's lanes rebuild its weights from the staged exponents inside the loop
-template <int MB, int KW, int FMT, bool VT>
+// A verbatim step's lanes rebuild its weights from the staged exponents inside the loop.  (Counting verbatim blocks
+// as zero weights and adding their products after the loop would be cheaper at small B, but X is the MMA's operand
+// for all eight rows, so a zero weight would meet an infinite activation as 0 * inf = NaN.)
+template <int MB, int KW, int FMT>
 __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant__ MmaArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -238,7 +238,6 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
     uint64_t *full = (uint64_t *)(smem + TB);                          // [stages]
     uint64_t *empty = full + a.stages;                                 // [stages]
     uint64_t *vfull = empty + a.stages;                                // staged verbatim exponents landed
-    uint8_t *zrow = smem + TB + 512;                                   // [128] zeros: verbatim steps' table row
     float *part = (float *)(smem + TB + 1024);                         // [blocks_cta * 8][B]
     const int part_bytes = (a.blocks_cta * kRowsPerStage * (int)a.B * 4 + 1023) / 1024 * 1024;
     const int bm_bytes = (a.bm_words * 4 + 1023) / 1024 * 1024;
@@ -326,9 +325,7 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
         }
     }
     for (int i = ctid; i < a.blocks_cta * kRowsPerStage * (int)a.B; i += C * 32) part[i] = 0.f;
-    if (ctid < 32) ((uint32_t *)zrow)[ctid] = 0u;
     const uint8_t *tab_lane = tab + 4 * lane;
-    const uint8_t *zero_lane = zrow + 4 * lane;
     const int cw = warp - 1;
     const int g = lane >> 2, t = lane & 3;
     const int kw0 = cw * KW;  // the warp's K range within the slice
@@ -402,16 +399,11 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
             const uint64_t w2 = ((uint64_t)bm[(bl0 >> 5) + 1] << 32) | bm[bl0 >> 5];
             vwin = (uint32_t)(w2 >> (bl0 & 31)) & ((1u << NJ) - 1u);
         }
-        if (kEarly) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
+        if (kEarly) release_slot(&empty[slot], lane);
 
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        // The lane's steps.  VB: some lane of the warp has a verbatim step.  With VT a verbatim step (its codes are
-        // all zero) reads a zero table row under a zero sign+mantissa mask, so its weights are exactly +0 (the
-        // verbatim pass after the main loop adds the block's true product); without VT its lanes rebuild the
-        // weights from the block's exponents.  The warp is converged again for the MMAs.
+        // The lane's steps.  VB: some lane of the warp has a verbatim step; its lanes rebuild that step's weights
+        // from the block's exponents.  The warp is converged again for the MMAs.
         auto run_steps = [&](auto VB) {
             constexpr bool vb = decltype(VB)::value;
 #pragma unroll
@@ -419,7 +411,7 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
                 if (k0 + kw0 + 64 * j >= K) continue;  // past the end of K (last slice; warp-uniform)
                 if (!kEarly) load_step(j, d0[j], d1[j]);
                 uint32_t pw[8];  // pairs of weights 16t + 2q, 16t + 2q + 1 of the step
-                if (FMT == FMT_PAL && vb && !VT && ((vwin >> j) & 1u)) {
+                if (FMT == FMT_PAL && vb && ((vwin >> j) & 1u)) {
                     if (!vx_ready) {  // first verbatim block met by this lane: the staged run must have landed
                         if (!mbar_wait(vfull, 0)) ok = false;
                         const uint64_t fb = (uint64_t)r0 * KB;
@@ -440,16 +432,13 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
                     for (int q = 0; q < 4; q++)
                         pairs_from_exps(word_of(d0[j], q), word_of(ev, q), pw[2 * q], pw[2 * q + 1]);
                 } else if (FMT == FMT_PAL) {
-                    const bool vj = vb && VT && ((vwin >> j) & 1u);
-                    const uint8_t *tl = vj ? zero_lane : tab_lane;
-                    const uint32_t msk = vj ? 0u : 0x807F807Fu;
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const uint32_t S = word_of(d0[j], q);
                         const uint32_t Cw = q < 2 ? d1[j].x : d1[j].y;
                         const int jb = 2 * (q & 1);
-                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & msk) | pair_exp(tl, Cw, jb);
-                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & msk) | pair_exp(tl, Cw, jb + 1);
+                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb);
+                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb + 1);
                     }
                 } else if (FMT == FMT_EXP) {
 #pragma unroll
@@ -459,19 +448,16 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
 #pragma unroll
                     for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[j], q); pw[4 + q] = word_of(d1[j], q); }
                 }
-                if (FMT == FMT_PAL && vb && !VT) __syncwarp();  // after the per-lane verbatim branch
+                if (FMT == FMT_PAL && vb) __syncwarp();  // after the per-lane verbatim branch
 #pragma unroll
                 for (int s = 0; s < 4; s++)
                     mma16816(acc, xa[j][2 * s], MB == 2 ? xb[MB == 2 ? j : 0][2 * s] : 0u, xa[j][2 * s + 1],
                              MB == 2 ? xb[MB == 2 ? j : 0][2 * s + 1] : 0u, pw[2 * s], pw[2 * s + 1]);
             }
         };
-        if (FMT == FMT_PAL && (!VT || __any_sync(__activemask(), vwin != 0))) run_steps(std::true_type{});
+        if (FMT == FMT_PAL && __any_sync(__activemask(), vwin != 0)) run_steps(std::true_type{});
         else run_steps(std::false_type{});
-        if (!kEarly) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
+        if (!kEarly) release_slot(&empty[slot], lane);
         // acc: rows row_base + 2t, 2t + 1 of batch rows g (acc[0..1]) and g + 8 (acc[2..3])
 #pragma unroll
         for (int m = 0; m < MB; m++) {
@@ -481,54 +467,6 @@ __global__ void __launch_bounds__(544, 1) gemv_mma_kernel(const __grid_constant_
                 const int64_t rw = row_base + 2 * t + e;
                 if (b < a.B && rw < r1) atomicAdd(&part[(rw - r0) * a.B + b], acc[2 * m + e]);
             }
-        }
-    }
-    // Verbatim blocks: the main loop counted each as zero; add their true products.  Work item (v, b) is the
-    // CTA's v-th verbatim block against batch row b; the block's exponents come from the staged run (or global
-    // memory beyond it), its sign+mantissa bytes and X from global memory.
-    if (FMT == FMT_PAL && VT && nrows && ok) {
-        const uint64_t fb = (uint64_t)r0 * KB, lb = (uint64_t)r1 * KB;
-        const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
-        const uint64_t lw = (lb >> 5) - wb0;
-        const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
-                                                    : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
-        const uint32_t v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
-        if (v_staged && !mbar_wait(vfull, 0)) ok = false;
-        const uint64_t items = (v_end - v_begin) * (uint64_t)a.B;
-        const uint64_t pol_x = l2_evict_last();
-        for (uint64_t it = ctid; it < items && ok; it += C * 32) {
-            const uint64_t v = v_begin + it / a.B;
-            const int64_t b = (int64_t)(it % a.B);
-            int lo = 0, hi = n_bw - 1;  // the last word whose prefix count is <= v
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if ((uint64_t)pf[mid] <= v) lo = mid;
-                else hi = mid - 1;
-            }
-            const int bit = (int)__fns(bm[lo], 0, (int)(v - pf[lo]) + 1);
-            const uint32_t blk = (uint32_t)((wb0 + lo) * 32) + (uint32_t)bit;  // (blocks of a matrix fit 32 bits)
-            const uint32_t row = blk / (uint32_t)KB;
-            const int64_t kb = (int64_t)(blk - row * (uint32_t)KB) * 64;
-            if (bit > 31 || kb < k0 || kb >= k0 + a.klen) continue;  // another K-slice's block
-            const uint64_t vl = v - v_begin;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int p = 0; p < 4; p++) {
-                const uint4 ev = vl < v_staged ? *(const uint4 *)(vx + vl * 64 + 16 * p)
-                                               : __ldg((const uint4 *)(a.w.verb_exp + v * 64 + 16 * p));
-                const uint4 sv = __ldg((const uint4 *)(a.w.sm + (uint64_t)blk * 64 + 16 * p));
-                const uint4 *xp = (const uint4 *)(a.x + b * K + kb + 16 * p);
-                const uint4 x0 = ldg_hint(xp, pol_x), x1 = ldg_hint(xp + 1, pol_x);
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    uint32_t p01, p23;
-                    pairs_from_exps(word_of(sv, q), word_of(ev, q), p01, p23);
-                    const uint4 &xv = q < 2 ? x0 : x1;
-                    s0 = fma2_bf16(p01, word_of(xv, 2 * (q & 1)), s0);
-                    s1 = fma2_bf16(p23, word_of(xv, 2 * (q & 1) + 1), s1);
-                }
-            }
-            atomicAdd(&part[(int64_t)(row - r0) * a.B + b], s0 + s1);
         }
     }
     if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
@@ -551,12 +489,8 @@ struct MmaShape {
 // 16 consumer warps, one CTA per SM; each warp owns 256 / MB (variant 6) or 128 (variant 7) weights of a slice
 int mma_kw(int64_t B, int variant) { return variant == 7 || B > 8 ? 128 : 256; }
 
-// 4-bit codes only: with the exponent-byte workspace of the exponent-only pipeline this kernel once returned
-// wrong rows on the 8B gate_proj at B = 16 (K split in two); until the cause is found the workspace formats run on
-// the plain-load GEMV or the tcgen05 kernels.
 bool plan_mma(const WOperand &w, int64_t B, int split_k, int variant, MmaShape &s)
 {
-    if (w.fmt != FMT_PAL) return false;
     if (B < 1 || B > 16 || w.K <= 0 || w.K % 256 || w.N <= 0) return false;
     if (!tensor_map_encoder()) return false;
     s.consumers = 16;
@@ -604,12 +538,12 @@ bool make_mma_maps(const WOperand &w, const MmaShape &s, CUtensorMap &m0, CUtens
     return make(m0, w.w, 2 * K, 64);
 }
 
-template <int MB, int KW, int FMT, bool VT>
+template <int MB, int KW, int FMT>
 cudaError_t launch_mma_one(const MmaArgs &a, dim3 grid, int threads, size_t smem, cudaStream_t st)
 {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<MB, KW, FMT, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<MB, KW, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              227 * 1024);
         if (e != cudaSuccess) return e;
         attr = true;
@@ -624,17 +558,15 @@ cudaError_t launch_mma_one(const MmaArgs &a, dim3 grid, int threads, size_t smem
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<MB, KW, FMT, VT>, a);
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<MB, KW, FMT>, a);
 }
 
 template <int MB, int KW>
 cudaError_t launch_mma_fmt(int fmt, const MmaArgs &a, dim3 grid, int threads, size_t smem, cudaStream_t st)
 {
-    // the verbatim pass after the main loop handles (block, batch row) pairs: cheap for small B only
-    if (fmt == FMT_PAL) return a.B <= 4 ? launch_mma_one<MB, KW, FMT_PAL, true>(a, grid, threads, smem, st)
-                                        : launch_mma_one<MB, KW, FMT_PAL, false>(a, grid, threads, smem, st);
-    if (fmt == FMT_EXP) return launch_mma_one<MB, KW, FMT_EXP, false>(a, grid, threads, smem, st);
-    return launch_mma_one<MB, KW, FMT_BF16, false>(a, grid, threads, smem, st);
+    if (fmt == FMT_PAL) return launch_mma_one<MB, KW, FMT_PAL>(a, grid, threads, smem, st);
+    if (fmt == FMT_EXP) return launch_mma_one<MB, KW, FMT_EXP>(a, grid, threads, smem, st);
+    return launch_mma_one<MB, KW, FMT_BF16>(a, grid, threads, smem, st);
 }
 
 }  // namespace

@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
                 for (int q = 0; q < 4; q++) mma16816(acc[n], p0[2 * q], p1[2 * q], p0[2 * q + 1], p1[2 * q + 1], xv[2 * q], xv[2 * q + 1]);
             }
         }
+        // the stage was read with generic-proxy loads and the next tensor copy into it writes through the async
+        // proxy: each lane fences its reads across the proxies before the warp hands the stage back
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (++kq == upk) { kq = 0; tile++; }

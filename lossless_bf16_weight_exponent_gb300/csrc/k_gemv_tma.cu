@@ -20,12 +20,15 @@
 // exponent fields of a bf16x2 pair from a 32 KB per-lane table in shared memory,
 // so a warp's lookups never share a bank.  A stage without verbatim blocks runs a
 // straight-line body; a verbatim block's codes are all zero, so reading a zero table
-// row under a zero sign+mantissa mask makes it add exactly +0 * x, and after the main
+// row under a zero sign+mantissa mask, with its activations masked to zero as well,
+// makes it add exactly +0 * +0 (even for an infinite activation), and after the main
 // loop the consumers add the CTA's verbatim blocks' true products from records staged
 // in shared memory and X written into the freed ring - no warp runs a slower body that
 // would hold the ring back.  Lane sums of four consecutive stages
 // are reduced together (a transposed butterfly), and row sums meet in shared
-// memory and are written once at the end.  Every
+// memory and are written once at the end.  A warp hands a slot back only after a
+// cross-proxy fence on its reads (the next bulk copy writes it through the async
+// proxy).  Every
 // mbarrier wait is bounded by a global-timer limit; on expiry the kernel latches
 // DEV_TIMEOUT, drains the copies it issued and returns.
 #include <cuda.h>
@@ -103,6 +106,19 @@ __device__ __forceinline__ uint64_t global_ns()
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
+}
+
+// Hand a ring slot back to the producer once the warp has read it.  The slot was read with generic-proxy loads
+// and is refilled by the bulk-copy engine, which writes through the async proxy; the PTX memory model orders a
+// thread's generic accesses before a later async-proxy access to the same bytes only through a proxy fence.  So
+// every lane fences its own reads, the warp converges, and one lane arrives on the slot's "empty" barrier.
+// Without the fence the next copy into the slot intermittently landed before a warp's loads had read it (wrong
+// rows in about 3% of full-decode runs on the 8B gate_proj, always in a warp that released its slot early).
+__device__ __forceinline__ void release_slot(uint64_t *empty_bar, int lane)
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);
 }
 
 // Wait until the barrier's phase with this parity completes; false after kWaitLimitNs.
@@ -461,18 +477,16 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 }
             }
         }
-        if (kEarly) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
+        if (kEarly) release_slot(&empty[slot], lane);
 
         float acc0[NB], acc1[NB];
 #pragma unroll
         for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
         // The lane's groups of this stage.  BD: some group of the warp lies past the CTA's rows or the K-slice
         // (those are skipped).  VB: some lane of the warp has a verbatim group; a verbatim group (its codes are
-        // all zero) reads a zero table row under a zero sign+mantissa mask, so it adds exactly +0 * x (the
-        // verbatim warp adds its true product).  Without BD the groups are straight-line code.
+        // all zero) reads a zero table row under a zero sign+mantissa mask and multiplies zero activations, so it
+        // adds exactly +0 * +0 even where X holds an infinity or a NaN (the pass after the main loop adds its
+        // true product).  Without BD the groups are straight-line code.
         auto run_groups = [&](auto BD, auto VB) {
             constexpr bool bd = decltype(BD)::value, vb = decltype(VB)::value;
 #pragma unroll
@@ -480,8 +494,9 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 if (bd && (!live || kbase + 512 * g >= klen)) continue;  // past the CTA's rows or the K-slice
                 if (!kEarly) load_group(g, d0[g], d1[g]);
                 uint32_t pw[8];  // 8 bf16x2 pairs of weights
+                bool vg = false;
                 if (FMT == FMT_PAL) {
-                    const bool vg = vb && ((vwin >> (8 * g)) & 1u);
+                    vg = vb && ((vwin >> (8 * g)) & 1u);
                     const uint8_t *tl = vg ? zero_lane : tab_lane;
                     const uint32_t msk = vg ? 0u : 0x807F807Fu;
 #pragma unroll
@@ -500,12 +515,13 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
 #pragma unroll
                     for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[g], q); pw[4 + q] = word_of(d1[g], q); }
                 }
+                const uint32_t xm = vg ? 0u : 0xFFFFFFFFu;  // (all ones unless the body handles verbatim groups)
 #pragma unroll
                 for (int j = 0; j < NB; j++)
 #pragma unroll
                     for (int t = 0; t < 8; t += 2) {
-                        acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
-                        acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
+                        acc0[j] = fma2_bf16(pw[t], vb ? xr[j][8 * g + t] & xm : xr[j][8 * g + t], acc0[j]);
+                        acc1[j] = fma2_bf16(pw[t + 1], vb ? xr[j][8 * g + t + 1] & xm : xr[j][8 * g + t + 1], acc1[j]);
                     }
             }
         };
@@ -518,10 +534,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         } else {
             run_groups(std::true_type{}, std::true_type{});
         }
-        if (!kEarly) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
+        if (!kEarly) release_slot(&empty[slot], lane);
         // shift the lane sum in; every fourth stage (and after the last) reduce four stages at once
 #pragma unroll
         for (int j = 0; j < NB; j++) {
@@ -786,14 +799,10 @@ bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaSha
 
 }  // namespace
 
-// 4-bit codes only.  With the bf16 workspace of the full-decode pipeline this kernel returned wrong values on a
-// few scattered rows in most runs on the 8B gate_proj (K split in two), with the workspace itself correct
-// afterwards and with kernels serialized as well; the exponent-byte workspace ran clean in the same test.  Until
-// the cause is found, both workspace formats run on the plain-load GEMV.
 bool gemv_tma_supported(const WOperand &w, int64_t B, int variant)
 {
     TmaShape s;
-    return w.fmt == FMT_PAL && variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
+    return variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
            plan_variant(w, B, 0, variant, s);
 }
 
@@ -801,7 +810,7 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
                     float *acc_ws, int *status, void *stream)
 {
     TmaShape s;
-    if (w.fmt != FMT_PAL || !plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
+    if (!plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
     const int nb = B <= 1 ? 1 : 2;
     cudaStream_t st = (cudaStream_t)stream;
     TmaArgs a;

@@ -507,14 +507,11 @@ cudaError_t launch_fmt(const TcArgs &a, dim3 grid, size_t smem, cudaStream_t st)
 
 }  // namespace
 
-// Variant 2: the tensor-memory kernel (k_tc2.cu) where it fits (B <= 256); variant 3: the persistent one
-// (k_tc3.cu, B <= 256, K % 256 == 0); variant 4: the persistent one with the rebuilt weights in shared memory
-// (k_tc4.cu, B <= 512, 4-bit codes, K % 256 == 0); any other variant or shape: this one.
+// Variant 4: the persistent kernel with the rebuilt weights in shared memory (k_tc4.cu, B <= 512, 4-bit codes,
+// K % 256 == 0); any other variant or shape: this one.
 bool tc_supported(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
-    if (variant == 2 && tc2_supported(w, B)) return true;
-    if (variant == 3 && tc3_supported(w, B)) return true;
     if (variant == 4 && tc4_supported(w, B)) return true;
     return encode_fn() != nullptr && tc_shape(w, B, 0, s);
 }
@@ -522,8 +519,6 @@ bool tc_supported(const WOperand &w, int64_t B, int variant)
 int tc_default_split(const WOperand &w, int64_t B, int variant)
 {
     TcShape s;
-    if (variant == 2 && tc2_supported(w, B)) return tc2_default_split(w, B);
-    if (variant == 3 && tc3_supported(w, B)) return 1;
     if (variant == 4 && tc4_supported(w, B)) return 1;
     return tc_shape(w, B, 0, s) ? s.nsplit : 1;
 }
@@ -531,8 +526,6 @@ int tc_default_split(const WOperand &w, int64_t B, int variant)
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream)
 {
-    if (variant == 2 && tc2_supported(w, B)) return launch_tc2(w, x, B, y, out_bf16, split_k, acc_ws, stream);
-    if (variant == 3 && tc3_supported(w, B)) return launch_tc3(w, x, B, y, out_bf16, acc_ws, stream);
     if (variant == 4 && tc4_supported(w, B)) {
         const int e = launch_tc4(w, x, B, y, out_bf16, acc_ws, stream);
         if (e != cudaErrorInvalidValue) return e;  // else: no tensor map for these operands, use this kernel

@@ -133,14 +133,6 @@ int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);
 bool tc_supported(const WOperand &w, int64_t B, int variant);
-// tcgen05 GEMM with the rebuilt weights in tensor memory (B <= 256): tensor-core variant 2
-bool tc2_supported(const WOperand &w, int64_t B);
-int tc2_default_split(const WOperand &w, int64_t B);
-int launch_tc2(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, float *acc_ws,
-               void *stream);
-// persistent tcgen05 GEMM (one CTA per SM over balanced 128 x 256 units; B <= 256, K % 256 == 0): variant 3
-bool tc3_supported(const WOperand &w, int64_t B);
-int launch_tc3(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
 int gemv_default_split(const WOperand &w, int64_t B);
 int tc_default_split(const WOperand &w, int64_t B, int variant);
 int num_sms();

@@ -9,10 +9,12 @@
 // needs one, the fp32 accumulator) lives in the array below, which the driver
 // places on every device that loads this library and keeps there until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "uw_internal.h"
 
@@ -22,28 +24,61 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[UW_NOALLOC_SCRATCH_BY
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+// The array's device address belongs to the CUDA context that loaded this module: the device's primary context,
+// or a context a driver-API caller created.  After cudaDeviceReset the primary context is a new one, and the
+// module (with the array) is loaded again, possibly elsewhere.  So the address is looked up once per context and
+// cached under the context's unique id (cuCtxGetId: never reused within the process).
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+std::vector<ScratchEntry> g_cache;
 
-// Device address of the scratch array on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// The current context's unique id; false if there is no current context or the driver lacks cuCtxGetId.
+bool current_context_id(unsigned long long *id)
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = (CtxGetCurrentFn)p;
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = (CtxGetIdFn)p;
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context.  In host code the array's name is only a host-side
+// stand-in, so the address comes from cudaGetSymbolAddress, with the context current; it is cached per context.
+// Without cuCtxGetId (a driver older than CUDA 12) every call looks it up again.
 uw_status scratch_address(void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return uw::fail(UW_ERR_CUDA, "uw_matmul_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return uw::fail(UW_ERR_UNSUPPORTED, "uw_matmul_noalloc: device %d", dev);
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
     std::lock_guard<std::mutex> g(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p)
-            return uw::fail(UW_ERR_CUDA, "uw_matmul_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    if (have_id)
+        for (const ScratchEntry &e : g_cache)
+            if (e.ctx_id == id) { *out = e.ptr; return UW_OK; }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+        return uw::fail(UW_ERR_CUDA, "uw_matmul_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    // the lookup above made the device's primary context current if no context was: take its id now
+    if (!have_id) have_id = current_context_id(&id);
+    if (have_id) g_cache.push_back(ScratchEntry{id, p});
+    *out = p;
     return UW_OK;
 }
 

@@ -198,7 +198,7 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
 extern "C" void uw_free(uw_matrix *m)
 {
     if (!m) return;
-    cudaDeviceSynchronize();
+    // no device-wide synchronisation of its own: cudaFree already waits for work still using the allocation
     cudaFree(m->dev);
     delete m;
 }
@@ -648,6 +648,7 @@ extern "C" uw_status uw_autotune(uw_matrix *m, const int64_t *batches, int n, vo
                 if (coord == 0) { for (int v = UW_STRAT_FULL_DECODE; v <= UW_STRAT_HUFFMAN_DIRECT; v++) if (strategy_ok(m, v)) values.push_back(v); }
                 else if (coord == 1) values = {UW_KERNEL_GEMV, UW_KERNEL_TC};
                 else if (coord == 2) values = split_candidates(m);
+                else if (best.kernel == UW_KERNEL_TC) values = {0, 4};
                 else values = {0, 1, 2, 3, 4, 5, 6, 7, 8};
                 for (int v : values) {
                     uw_plan p = best;

@@ -13,7 +13,7 @@ import pytest
 import lossless_bf16_weight_exponent_gb300 as uw
 import oracle
 import synth
-from uwtest import dev_bytes, run_matmul, strategies_for, to_dev_u16, tol_ok, torch
+from uwtest import check_rows, dev_bytes, oracle_ref, pick, run_matmul, strategies_for, to_dev_u16, tol_ok, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -59,35 +59,33 @@ def test_palette_high_exponents_present():
 
 @pytest.mark.parametrize("B", [1, 3, 8, 9, 16])
 @pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
-def test_mma_gemv_gate_8b_sampled(B, out_dtype):
-    # the tensor-pipe GEMV at full size, in the launch shapes the autotuner chooses from, on sampled rows
+def test_mma_gemv_gate_8b(B, out_dtype):
+    # the tensor-pipe GEMV at full size, in the launch shapes the autotuner chooses from
     mat = synth.gate_8b()
     w = mat.weights()
     x = mat.activations(B)
-    rng = np.random.default_rng(B)
-    rows = np.unique(np.concatenate([[0, 7, 8, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=B)
+    yref, absum = oracle_ref("gate_8b", w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
     for v in (6, 7):
-        y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_GEMV, 0, v), out_dtype)[:, rows]
+        y = pick(run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_GEMV, 0, v), out_dtype), rows)
         ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
         assert ok, (v, worst)
 
 
 @pytest.mark.parametrize("B", [1, 4, 16, 17, 32, 33, 48, 64])
 @pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
-def test_rp_gemv_gate_8b_sampled(B, out_dtype):
-    # the row-parallel tensor-pipe GEMV (variant 8) at full size on sampled rows, from both weight forms:
-    # resident codes (direct palette) and codes transcoded from the Huffman stream into the workspace
+def test_rp_gemv_gate_8b(B, out_dtype):
+    # the row-parallel tensor-pipe GEMV (variant 8) at full size, from both weight forms: resident codes (direct
+    # palette) and codes transcoded from the Huffman stream into the workspace
     mat = synth.gate_8b()
     w = mat.weights()
     x = mat.activations(B)
-    rng = np.random.default_rng(100 + B)
-    rows = np.unique(np.concatenate([[0, 127, 128, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=100 + B)
+    yref, absum = oracle_ref("gate_8b", w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN), want_palette_form=True)
     for s in (uw.STRAT_DIRECT_PALETTE, uw.STRAT_PALETTE_TRANSCODE):
-        y = run_matmul(m, x, (s, uw.KERNEL_GEMV, 0, 8), out_dtype)[:, rows]
+        y = pick(run_matmul(m, x, (s, uw.KERNEL_GEMV, 0, 8), out_dtype), rows)
         ok, worst = tol_ok(y, yref, absum, out_dtype == uw.OUT_BF16)
         assert ok, (s, worst)
 
@@ -99,12 +97,12 @@ def test_split_target_zeroed_before_the_dependent_launch_adds():
     t = torch()
     mat = synth.gate_8b()
     w = mat.weights()
-    rows = np.unique(np.concatenate([[0, 1, mat.N - 1], np.random.default_rng(2).choice(mat.N, 61, replace=False)]))
     m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN), want_palette_form=True)
     for B, plans in ((1, [(s, uw.KERNEL_GEMV, 2, 4) for s in (1, 2, 3, 4)]),
                      (16, [(s, uw.KERNEL_GEMV, 2, 6) for s in (1, 2, 3, 4)])):
         x_np = mat.activations(B)
-        yref, absum = oracle.matmul(w, x_np, rows)
+        rows = check_rows(mat.N, B, seed=2)
+        yref, absum = oracle_ref("gate_8b", w, x_np, rows)
         x = to_dev_u16(x_np)
         y = t.empty((B, mat.N), dtype=t.float32, device="cuda")
         for p in plans:
@@ -115,6 +113,6 @@ def test_split_target_zeroed_before_the_dependent_launch_adds():
                 y.fill_(3.0e30)
                 m.matmul_plan(x, B, y, plan, uw.OUT_F32, ws, need)
                 t.cuda.synchronize()
-                got = y.cpu().numpy().astype(np.float64)[:, rows]
+                got = pick(y.cpu().numpy().astype(np.float64), rows)
                 ok, worst = tol_ok(got, yref, absum)
                 assert ok, (p, worst)

@@ -1,6 +1,6 @@
 """GPU parity of the Huffman-direct GEMV (the GEMV that decodes the Huffman stream itself) against the
 oracle's fp64 contraction: chunk sizes and code-length limits, ragged row counts, verbatim-heavy and
-single-symbol matrices, exact integer cases, fp32 and bf16 outputs, full-size 8B and 70B shapes on sampled rows,
+single-symbol matrices, exact integer cases, fp32 and bf16 outputs, full-size 8B and 70B shapes on every row,
 corrupt streams, and the cases the strategy does not take.  Cloudflare blog "Unweight": the section on the
 execution pipelines (the Huffman-fed pipelines) and the section on the decode kernels (lookup table in shared
 memory)."""
@@ -10,7 +10,7 @@ import pytest
 import lossless_bf16_weight_exponent_gb300 as uw
 import oracle
 import synth
-from uwtest import dev_bytes, run_matmul, tol_ok, to_dev_u16, torch
+from uwtest import check_rows, dev_bytes, oracle_ref, pick, run_matmul, tol_ok, to_dev_u16, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -155,40 +155,34 @@ def test_corrupt_stream_latched():
         m.check()
 
 
-def _sampled_rows(N, seed):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, 1, 31, 32, N - 2, N - 1], rng.choice(N, 122, replace=False)]))
-
-
 @pytest.mark.parametrize("B", [1, 4, 8])
-def test_gate_8b_full_size_sampled(B):
+def test_gate_8b_full_size(B):
     mat = synth.gate_8b()
     w = mat.weights()
     x = mat.activations(B)
-    rows = _sampled_rows(mat.N, B)
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=B)
+    yref, absum = oracle_ref("gate_8b", w, x, rows)
     m = _huffman_only(w)
-    y = run_matmul(m, x, uw.STRAT_AUTO)[:, rows]
+    y = pick(run_matmul(m, x, uw.STRAT_AUTO), rows)
     ok, worst = tol_ok(y, yref, absum)
     assert ok, worst
-    y = run_matmul(m, x, HD, uw.OUT_BF16)[:, rows]
+    y = pick(run_matmul(m, x, HD, uw.OUT_BF16), rows)
     assert tol_ok(y, yref, absum, True)[0]
-    y = run_matmul(m, x, (HD, uw.KERNEL_GEMV, 0, 1))[:, rows]
+    y = pick(run_matmul(m, x, (HD, uw.KERNEL_GEMV, 0, 1)), rows)
     assert tol_ok(y, yref, absum)[0]
     m.check()
 
 
 @pytest.mark.parametrize("which", ["down", "gate"])
-def test_70b_shapes_sampled(which):
+def test_70b_shapes(which):
     mats = {mm.name.split(".")[-1]: mm for mm in synth.mlp_70b()}
     mat = mats[which]
     w = mat.weights()
     x = mat.activations(1)
-    rows = _sampled_rows(mat.N, 7)
-    yref, absum = oracle.matmul(w, x, rows)
+    yref, absum = oracle_ref("70b_" + which, w, x)
     m = _huffman_only(w)
     for p in (HD, (HD, uw.KERNEL_GEMV, 0, 1)):
-        y = run_matmul(m, x, p)[:, rows]
+        y = run_matmul(m, x, p)
         ok, worst = tol_ok(y, yref, absum)
         assert ok, (p, worst)
     m.check()

@@ -1,14 +1,15 @@
 """GPU parity: uw_matmul against the oracle's fp64 contraction, for every
 strategy (the four pipelines of the Cloudflare blog "Unweight"), every kernel,
 ragged shapes and batch sizes, fp32 and bf16 outputs; full-size configurations
-are checked on sampled rows in the launch configuration the bench times."""
+are checked on every row up to B = 4 and on 1024+ rows spread over every CTA's range beyond, in the launch
+configuration the bench times."""
 import numpy as np
 import pytest
 
 import lossless_bf16_weight_exponent_gb300 as uw
 import oracle
 import synth
-from uwtest import dev_bytes, run_matmul, strategies_for, tol_ok, to_dev_u16, torch
+from uwtest import check_rows, dev_bytes, oracle_ref, pick, run_matmul, strategies_for, tol_ok, to_dev_u16, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -100,37 +101,32 @@ def test_error_paths():
     assert e.value.status == uw.ERR_SHAPE
 
 
-def _sampled_rows(N, seed):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, 1, N - 2, N - 1], rng.choice(N, 124, replace=False)]))
-
-
 @pytest.mark.parametrize("B", [1, 4, 16])
-def test_gate_8b_full_size_sampled(B):
+def test_gate_8b_full_size(B):
     mat = synth.gate_8b()
     w = mat.weights()
     x = mat.activations(B)
-    rows = _sampled_rows(mat.N, B)
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=B)
+    yref, absum = oracle_ref("gate_8b", w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN), want_palette_form=True)
     for s in strategies_for(m):
-        y = run_matmul(m, x, s)[:, rows]
+        y = pick(run_matmul(m, x, s), rows)
         ok, worst = tol_ok(y, yref, absum)
         assert ok, (s, worst)
-    y = run_matmul(m, x, uw.STRAT_AUTO, uw.OUT_BF16)[:, rows]
+    y = pick(run_matmul(m, x, uw.STRAT_AUTO, uw.OUT_BF16), rows)
     assert tol_ok(y, yref, absum, True)[0]
 
 
 @pytest.mark.parametrize("which,B", [("down", 1), ("gate", 1), ("down", 32)])
-def test_70b_shapes_sampled(which, B):
+def test_70b_shapes(which, B):
     mats = {m.name.split(".")[-1]: m for m in synth.mlp_70b()}
     mat = mats[which]
     w = mat.weights()
     x = mat.activations(B)
-    rows = _sampled_rows(mat.N, B + 1)
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=B + 1)
+    yref, absum = oracle_ref("70b_" + which, w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
-    y = run_matmul(m, x, uw.STRAT_DIRECT_PALETTE)[:, rows]
+    y = pick(run_matmul(m, x, uw.STRAT_DIRECT_PALETTE), rows)
     ok, worst = tol_ok(y, yref, absum)
     assert ok, worst
 

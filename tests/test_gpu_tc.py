@@ -1,16 +1,16 @@
 """GPU parity of the tcgen05 tensor-core kernels against the oracle's fp64 contraction: variant 0 rebuilds
-into shared memory, variant 2 into tensor memory (the MMA's A operand), variant 3 is the persistent
-tensor-memory kernel over balanced 128 x 256 units, variant 4 the persistent kernel that rebuilds each 64-weight
-step into shared memory; all accumulate in fp32 in tensor memory.  Every weight format they consume (4-bit palette codes, exponent bytes, plain bf16 after full
-decode), ragged N (not a multiple of the 128-row tile), batch sizes from 1 to 512 (N-padding, two MMAs per
-K-step above 256), K-splits and both output dtypes."""
+each 128-row tile into shared memory, variant 4 is the persistent kernel over balanced 128 x 256 units that
+rebuilds each 64-weight step into shared memory; both accumulate in fp32 in tensor memory.  Every weight format
+they consume (4-bit palette codes, exponent bytes, plain bf16 after full decode), ragged N (not a multiple of the
+128-row tile), batch sizes from 1 to 512 (N-padding, two MMAs per K-step above 256), K-splits and both output
+dtypes; the full 8B gate_proj on every row up to B = 4 and 1024+ spread rows beyond."""
 import numpy as np
 import pytest
 
 import lossless_bf16_weight_exponent_gb300 as uw
 import oracle
 import synth
-from uwtest import run_matmul, tol_ok
+from uwtest import check_rows, oracle_ref, pick, run_matmul, tol_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +21,7 @@ def mats():
     return w, uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN, 256, 12), want_palette_form=True)
 
 
-@pytest.mark.parametrize("variant", [0, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 4])
 @pytest.mark.parametrize("B", [1, 3, 16, 17, 100, 256, 300, 512])
 @pytest.mark.parametrize("strategy", [uw.STRAT_DIRECT_PALETTE, uw.STRAT_EXP_ONLY, uw.STRAT_FULL_DECODE,
                                       uw.STRAT_PALETTE_TRANSCODE])
@@ -34,7 +34,7 @@ def test_tc_all_formats(mats, B, strategy, variant):
     assert ok, worst
 
 
-@pytest.mark.parametrize("variant", [0, 2, 3, 4])
+@pytest.mark.parametrize("variant", [0, 4])
 @pytest.mark.parametrize("split", [2, 3, 16])
 @pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
 def test_tc_splits_and_bf16(mats, split, out_dtype, variant):
@@ -57,20 +57,19 @@ def test_tc_exact_integers():
     exact = Xi.astype(np.float64) @ Wi.astype(np.float64).T
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
     for s in (uw.STRAT_DIRECT_PALETTE, uw.STRAT_EXP_ONLY, uw.STRAT_FULL_DECODE):
-        for v in (0, 2, 3, 4):
+        for v in (0, 4):
             assert np.array_equal(run_matmul(m, x, (s, uw.KERNEL_TC, 1, v)), exact), (s, v)
 
 
 @pytest.mark.parametrize("B", [16, 64, 256, 512])
-def test_tc_gate_8b_sampled(B):
+def test_tc_gate_8b(B):
     mat = synth.gate_8b()
     w = mat.weights()
     x = mat.activations(B)
-    rng = np.random.default_rng(B)
-    rows = np.unique(np.concatenate([[0, 127, 128, mat.N - 1], rng.choice(mat.N, 60, replace=False)]))
-    yref, absum = oracle.matmul(w, x, rows)
+    rows = check_rows(mat.N, B, seed=B)
+    yref, absum = oracle_ref("gate_8b", w, x, rows)
     m = uw.Matrix(uw.encode(w, uw.CODEC_PALETTE))
-    for v in ((0, 2, 4) if B <= 256 else (0, 4)):
-        y = run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, v))[:, rows]
+    for v in (0, 4):
+        y = pick(run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, v)), rows)
         ok, worst = tol_ok(y, yref, absum)
         assert ok, (v, worst)

@@ -1,4 +1,5 @@
-"""Helpers shared by the GPU tests: device buffers and the matmul tolerance (1e-4 of sum |w x| plus 1e-6; 2^-7 relative added for bf16 output)."""
+"""Helpers shared by the GPU tests: device buffers, the matmul tolerance (1e-4 of sum |w x| plus 1e-6; 2^-7
+relative added for bf16 output), the rows a full-size parity test checks, and a cache of the oracle's results."""
 import numpy as np
 
 import lossless_bf16_weight_exponent_gb300 as uw
@@ -60,3 +61,32 @@ def strategies_for(m):
     if m.info["has_palette_form"]:
         out.append(uw.STRAT_DIRECT_PALETTE)
     return out
+
+
+def check_rows(N, B, seed=0):
+    """Rows a full-size parity test compares: every row when B <= 4 (the oracle's fp64 GEMV of the 8B gate_proj
+    takes about a second per batch row); otherwise one random row from each of 1024 equal bins of [0, N) plus the
+    first and last two rows, so every CTA's and every 128-row unit's row range is checked."""
+    if B <= 4 or N <= 2048:
+        return None
+    rng = np.random.default_rng(seed)
+    edges = np.linspace(0, N, 1025).astype(np.int64)
+    picks = [int(rng.integers(lo, hi)) for lo, hi in zip(edges[:-1], edges[1:]) if hi > lo]
+    return np.unique(np.array([0, 1, N - 2, N - 1] + picks, dtype=np.int64))
+
+
+_REF = {}
+
+
+def oracle_ref(key, w, x, rows=None):
+    """The oracle's (Y, sum |w x|) for these rows (None: all), cached by key so tests sharing a full-size
+    workload pay for its fp64 contraction once."""
+    k = (key, x.shape[0], None if rows is None else rows.tobytes())
+    if k not in _REF:
+        _REF[k] = oracle.matmul(w, x, rows)
+    return _REF[k]
+
+
+def pick(y, rows):
+    """Y restricted to the checked rows (all rows when rows is None)."""
+    return y if rows is None else y[:, rows]
