@@ -1,12 +1,20 @@
 """Benchmark: fused decompress + matmul on the Llama-3.1-8B-shaped gate_proj W[14336,4096].
 
 One step = one uw_matmul of the autotuned plan (AUTO) at B=1 on a Huffman-coded
-matrix loaded with its resident palette form, i.e. one pass of the whole hot
-path: strategy lookup, (preprocess if the plan has one), on-chip BF16
-reconstruction and the contraction.  Inputs are larger than L2: the step rotates
-over several device copies of the compressed matrix (each copy its own uw_matrix),
-so every step streams its weights from HBM.  Steps are replayed through CUDA
-graphs captured from the same C-ABI calls.
+matrix held on the device as its 4-bit palette form (the stream is transcoded at
+load time and dropped), i.e. one pass of the whole hot path: strategy lookup,
+(preprocess if the plan has one), on-chip BF16 reconstruction and the
+contraction.  Inputs are larger than L2: the step rotates over several device
+copies of the compressed matrix (each copy its own uw_matrix), so every step
+streams its weights from HBM.  Steps are replayed through CUDA graphs captured
+from the same C-ABI calls.
+
+Timing: nvidia-smi samples the clocks from before an untimed load ramp; then,
+after a barrier and a synchronize, the stream is held at a device-side gate
+while the warm-up steps and the timed steps (between two CUDA events) are
+queued behind it, and the gate is opened.  So the GPU runs warm-up and timed
+steps back to back with no idle gap and no host launch latency inside the timed
+region; a synchronize and a barrier close it.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (the
 plain C decoder + fp64 matmul) on the host cores instead.
@@ -14,6 +22,9 @@ plain C decoder + fp64 matmul) on the host cores instead.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
+import ctypes
+import hashlib
 import json
 import os
 import statistics
@@ -29,12 +40,37 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 2 ** 20
 WORKLOAD = "gate_8b"
+CSRC = os.path.join(ROOT, "lossless_bf16_weight_exponent_gb300", "csrc")
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of that kernel as it stands
-# (profiles/launches_bench_gate8b_b1.md, profiles/gemv_mma_kernel_gate8b_b4.md). Keyed by (workload, batch,
-# kernel name); a kernel change invalidates it.
-MEASURED_TRAFFIC = {("gate_8b", 1, "gemv_tma_kernel"): 91.928320e6,
-                    ("gate_8b", 4, "gemv_mma_kernel"): 93.158400e6}
+# DRAM bytes (read + write) per launch of a kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by (workload, batch, kernel name), with the source file of the kernel and the first
+# 16 hex digits of its SHA-256 at capture time.  When the source has changed since, the figure no longer describes
+# the kernel and the line reports null.
+MEASURED_TRAFFIC = {}
+
+
+def source_sha16(fname):
+    try:
+        with open(os.path.join(CSRC, fname), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+
+
+KERNEL_SOURCE = {"gemv_tma_kernel": "k_gemv_tma.cu", "gemv_rp_kernel": "k_gemv_rp.cu", "gemv_mma_kernel": "k_gemv_mma.cu",
+                 "gemv_huff_kernel": "k_gemv_huff.cu", "gemv_kernel": "k_gemv.cu", "tc4_kernel": "k_tc4.cu",
+                 "tc_kernel": "k_tc.cu"}
+
+
+def measured_traffic(workload, B, kname):
+    """(bytes per launch, capture note) when a capture of this kernel as it stands exists, else (None, why)."""
+    e = MEASURED_TRAFFIC.get((workload, B, kname))
+    if e is None:
+        return None, "no ncu capture of this kernel and workload"
+    nbytes, fname, sha = e
+    if source_sha16(fname) != sha:
+        return None, f"{fname} changed since its ncu capture"
+    return nbytes, f"ncu capture of {kname} ({fname} sha256 {sha})"
 
 
 def kernel_name(plan, B):
@@ -63,16 +99,18 @@ def launches_per_call(plan, B):
     return pre + zero + 1
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--batch", type=int, default=1)
-    p.add_argument("--no-breakdown", action="store_true")
+    p.add_argument("--no-breakdown", action="store_true", help="skip the per-strategy and per-workload points")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-autotune", action="store_true")
+    p.add_argument("--points-budget", type=float, default=150.0,
+                   help="seconds the per-workload points may take (points past it are listed as skipped)")
     p.add_argument("--json-out", default=None)
     p.add_argument("--workload", default="gate_8b",
                    choices=["gate_8b", "down_8b", "gate_70b", "down_70b", "heavy_tail", "tiny"],
@@ -81,11 +119,11 @@ def parse():
     p.add_argument("--sweep", action="store_true",
                    help="time every configuration (tiny, 8B gate, 8B MLP stack, heavy tail, 70B gate/down) at each of "
                         "its batch sizes under the autotuned plan; one JSON line per (configuration, B)")
-    p.add_argument("--stack-layers", type=int, default=32, help="layers of the 8B MLP stack in --sweep")
-    p.add_argument("--resident", default="palette", choices=["palette", "huffman"],
-                   help="what stays resident: the Huffman blob with its palette form (default), or the Huffman blob "
-                        "alone (AUTO then decodes the stream inside the GEMV for B <= 8)")
-    return p.parse_args()
+    p.add_argument("--stack-layers", type=int, default=32, help="layers of the 8B MLP stack")
+    p.add_argument("--resident", default="palette", choices=["palette", "huffman", "both"],
+                   help="what stays resident of the Huffman blob: the palette form alone (default), the Huffman "
+                        "stream alone (AUTO then decodes the stream inside the GEMV for B <= 8), or both")
+    return p.parse_args(argv)
 
 
 def workload_matrix(name):
@@ -104,12 +142,14 @@ def workload_matrix(name):
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, which)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            "measured"
     except Exception:
-        return 6800.0, 1900.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 def algorithmic_bytes(info, strategy, B, out_bytes=4):
@@ -126,10 +166,10 @@ def algorithmic_bytes(info, strategy, B, out_bytes=4):
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """nvidia-smi sampling of SM and memory clocks and throttle reasons while the GPU works."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,clocks.mem,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -142,7 +182,14 @@ class Clocks:
                                        "-i", str(self.gpu), "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
-        time.sleep(0.3)
+            return
+        # until the first sample is written (or a second has passed)
+        t0 = time.time()
+        while time.time() - t0 < 1.0:
+            self.f.flush()
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.p is not None:
@@ -155,19 +202,61 @@ class Clocks:
         self.f.seek(0)
         rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm, mx, reasons = [], None, set()
+        sm, mem, mx, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
-                for nm, v in zip(names, r[5:9]):
+                sm.append(float(r[2]))
+                mx = float(r[3])
+                mem.append(float(r[4]))
+                for nm, v in zip(names, r[7:11]):
                     if v.strip().lower() == "active":
                         reasons.add(nm)
             except Exception:
                 pass
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "mem_mhz": statistics.median(mem) if mem else None, "reasons": sorted(reasons), "samples": len(sm),
+                "window": "from before the untimed load ramp to the end of the timed region"}
+
+
+class StreamGate:
+    """Holds a stream at a device-side wait (cuStreamWaitValue32 on a flag in device memory) until the host opens
+    it from a second stream, so that every launch of the timed region is queued before the first one runs."""
+    WAIT_GEQ, WRITE_DEFAULT = 0x0, 0x0
+
+    def __init__(self):
+        import torch
+        self.ok = False
+        try:
+            cu = ctypes.CDLL("libcuda.so.1")
+            self._wait = getattr(cu, "cuStreamWaitValue32_v2", None) or cu.cuStreamWaitValue32
+            self._write = getattr(cu, "cuStreamWriteValue32_v2", None) or cu.cuStreamWriteValue32
+            for f in (self._wait, self._write):
+                f.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint]
+                f.restype = ctypes.c_int
+            self.flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+            self.side = torch.cuda.Stream()
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def close(self, stream):
+        """Enqueue on `stream` a wait for the flag; False (and no wait) if the driver refuses it."""
+        import torch
+        if not self.ok:
+            return False
+        self.flag.zero_()
+        torch.cuda.synchronize()
+        if self._wait(ctypes.c_void_p(stream.cuda_stream), self.flag.data_ptr(), 1, self.WAIT_GEQ) != 0:
+            self.ok = False
+            return False
+        return True
+
+    def open(self):
+        import torch
+        if self._write(ctypes.c_void_p(self.side.cuda_stream), self.flag.data_ptr(), 1, self.WRITE_DEFAULT) != 0:
+            with torch.cuda.stream(self.side):
+                self.flag.fill_(1)
 
 
 def gpu_id(dev):
@@ -241,10 +330,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import lossless_bf16_weight_exponent_gb300 as uw
     import oracle
     import synth
     oracle.build()
+    synth.build()
     mat = synth.gate_8b()
     w = mat.weights()
     blob = oracle.encode(w, oracle.HUFFMAN)
@@ -269,214 +358,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# ------------------------------------------------------------------ GPU arm
-def run_ours(args):
-    import torch
-
+# ------------------------------------------------------------------ helpers of the GPU arm
+def load_copies(blob, resident, min_copies=2):
+    """Enough device copies of one matrix that a rotation over them streams from HBM (3x L2 at least)."""
     import lossless_bf16_weight_exponent_gb300 as uw
-    import synth
-
-    rank, world, local = dist_setup()
-    dev = torch.cuda.current_device()
-    B = args.batch
-    mat = workload_matrix(args.workload)
-    w = mat.weights()
-    blob = uw.encode(w, uw.CODEC_HUFFMAN)
-    pal_form = args.resident == "palette"
-    base = uw.Matrix(blob, want_palette_form=pal_form)
-    info = base.info
-    resident = info["device_bytes"]
-    copies = max(2, int(np.ceil(3 * L2_BYTES / max(1, resident))))
-    mats = [base] + [uw.Matrix(blob, want_palette_form=pal_form) for _ in range(copies - 1)]
-
-    # autotune on one copy (batches of the workload), share the table with the others
-    tune_batches = [1, 4, 16] if B in (1, 4, 16) else [B]
-    if args.plan:
-        vals = [int(v) for v in args.plan.split(",")]
-        text = "%d %d %d %d %d 0\n" % (1 << max(0, (B - 1).bit_length()), *vals)
-        for m in mats:
-            m.tune_load(text)
-    elif not args.no_autotune:
-        need = base.autotune_workspace_size(tune_batches)
-        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        base.autotune(tune_batches, tws, need)
-        del tws
-        table = base.tune_save()
-        for m in mats[1:]:
-            m.tune_load(table)
-    plan = base.plan_for(B)
-    ws_bytes = max(m.workspace_size(B) for m in mats)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
-    y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
-    stream = torch.cuda.Stream()
-
-    def step(i, s):
-        mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
-
-    # CUDA graphs of G steps each, replayed to reach exactly K steps
-    K, W = args.steps, args.warmup
-    G = min(64, K)
-    graphs = {}
-
-    def graph_for(n):
-        if n not in graphs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                for i in range(n):  # warm the plan outside capture once
-                    step(i, stream)
-                stream.synchronize()
-                with torch.cuda.graph(g, stream=stream):
-                    for i in range(n):
-                        step(i, stream)
-            graphs[n] = g
-        return graphs[n]
-
-    def run_steps(n):
-        full, rem = divmod(n, G)
-        gf = graph_for(G) if full else None
-        gr = graph_for(rem) if rem else None
-        with torch.cuda.stream(stream):
-            for _ in range(full):
-                gf.replay()
-            if gr is not None:
-                gr.replay()
-
-    run_steps(max(W, 3))
-    if K >= G:
-        graph_for(G)          # build every graph the timed region replays before timing starts
-    if K % G:
-        graph_for(K % G)
-    run_steps(min(K, G))
-    stream.synchronize()
-    clocks = Clocks(gpu_id(dev))
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    run_steps(K)
-    e1.record(stream)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
-    ms_step = ms_total / K
-
-    hbm_peak, tf_peak, peak_kind = peaks()
-    alg = algorithmic_bytes(info, plan.strategy, B)
-    eff_bytes = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
-    value = job_throughput(eff_bytes, K, world, ms_total)
-
-    launches_per_step = launches_per_call(plan, B)
-
-    # e2e through the public API with host buffers: H2D of X and D2H of Y inside the timed region
-    xh = torch.from_numpy(mat.activations(B).view(np.int16)).pin_memory()
-    yh = torch.empty((B, mat.N), dtype=torch.float32).pin_memory()
-    hneed = max(m.host_workspace_size(B) for m in mats)
-    hws = torch.empty(hneed, dtype=torch.uint8, device="cuda")
-    e2e_steps = min(max(K, 10), 2000)
-    for i in range(20):
-        mats[i % copies].matmul_host(xh, B, yh, uw.OUT_F32, hws, hneed, stream)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        mats[i % copies].matmul_host(xh, B, yh, uw.OUT_F32, hws, hneed, stream)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = job_throughput(eff_bytes, e2e_steps, world, e2e_s * 1e3)
-
-    breakdown = {}
-    if not args.no_breakdown and rank == 0 and args.workload == "gate_8b" and pal_form:
-        breakdown = strategy_breakdown(mats, mat, info, copies, hbm_peak)
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(blob, w, mat, B)
-
-    if rank == 0:
-        achieved = alg / (ms_step * 1e-3) / 1e9
-        kname = kernel_name(plan, B)
-        traffic = MEASURED_TRAFFIC.get((args.workload, B, kname))
-        line = {
-            "metric": "effective BF16 weight GB/s, fused decompress+matmul (B=%d)" % B,
-            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": max(W, 3),
-            "ms_per_step": ms_step, "us_per_matmul": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: W[{mat.N},{mat.K}] bf16 ({mat.name} recipe), "
-                                   + ("Huffman blob + resident palette form" if pal_form else "Huffman blob alone")
-                                   + f"; X[{B},{mat.K}] N(0,1)",
-                       "batch": B, "plan": plan.as_tuple(), "copies_rotated": copies,
-                       "l2": f"inputs larger than L2: {copies} copies x {resident / 1e6:.1f} MB resident",
-                       "compression": {"huffman_bits_per_weight": 8 * info["blob_bytes"] / (mat.N * mat.K),
-                                       "verbatim_block_fraction": info["n_verbatim"] / info["n_blocks"]}},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": alg, "kernel": kname},
-            "effective_frac_of_peak": value / world / hbm_peak,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * B * mat.K,
-                    "d2h_bytes_per_step": 4 * B * mat.N, "us_per_call": e2e_s / e2e_steps * 1e6},
-            "gpu_launches": launches_per_step * K,
-            "clocks": clk,
-            "cpu_baseline": cpu,
-            "breakdown": breakdown,
-        }
-        s = json.dumps(line)
-        print(s, flush=True)
-        if args.json_out:
-            with open(args.json_out, "w") as f:
-                f.write(s + "\n")
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    base = uw.Matrix(blob, resident=resident)
+    copies = min(64, max(min_copies, int(np.ceil(3 * L2_BYTES / max(1, base.info["device_bytes"])))))
+    return [base] + [uw.Matrix(blob, resident=resident) for _ in range(copies - 1)]
 
 
-def strategy_breakdown(mats, mat, info, copies, hbm_peak):
-    """Per (B, strategy) timing of single calls rotating the copies (eager launches, L2 not warm)."""
+def autotune_shared(mats, batches):
+    """Autotune the first copy for `batches` and share its table with the others."""
     import torch
-
-    import lossless_bf16_weight_exponent_gb300 as uw
-    out = {}
-    names = {1: "full_decode", 2: "exp_only", 3: "palette_transcode", 4: "direct_palette", 5: "huffman_direct"}
-    for B in (1, 4, 16):
-        x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
-        y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
-        eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
-        row = {}
-        for s, nm in names.items():
-            if s == 5 and B > 8:
-                continue  # the Huffman-direct GEMV takes B <= 8
-            if s == 4 and not mats[0].info["has_palette_form"]:
-                continue
-            need = mats[0].workspace_size(B, s)
-            ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
-            for i in range(6):
-                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
-            st = torch.cuda.current_stream()
-            reps = 40
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
-            for i in range(reps):
-                ev[2 * i].record(st)
-                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
-                ev[2 * i + 1].record(st)
-            torch.cuda.synchronize()
-            us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(reps))
-            alg = algorithmic_bytes(info, s, B)
-            row[nm] = {"us": round(us, 2), "eff_GBps": round(eff / us / 1e3, 1),
-                       "compressed_GBps": round(alg / us / 1e3, 1), "compressed_frac": round(alg / us / 1e3 / hbm_peak, 3)}
-        auto = mats[0].plan_for(B)
-        row["auto_plan"] = auto.as_tuple()
-        out[f"B={B}"] = row
-    return out
-
-
-def cpu_baseline(blob, w, mat, B):
-    x = mat.activations(B)
-    times = oracle_step_seconds(blob, w.shape, x, 2)
-    sec = sum(times) / len(times)
-    eff = (2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N) / sec / 1e9
-    return {"value": eff, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"2 full steps: plain-C decode of the Huffman blob + fp64 GEMV at B={B}"}
+    need = mats[0].autotune_workspace_size(batches)
+    tws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+    mats[0].autotune(batches, tws, need)
+    del tws
+    table = mats[0].tune_save()
+    for m in mats[1:]:
+        m.tune_load(table)
 
 
 def time_graph(fn, n, reps, stream):
@@ -504,83 +404,86 @@ def time_graph(fn, n, reps, stream):
     return statistics.median(ts)
 
 
-def run_sweep(args):
-    """Every configuration of the workload list at each of its batch sizes, autotuned plan, graph replays over
-    enough resident copies that a pass streams from HBM (except the tiny matrix, smaller than L2)."""
+def encode_many(recipes, threads=None):
+    """Blobs of many matrices, generated and encoded on a thread pool (both run in C with the GIL released)."""
+    import lossless_bf16_weight_exponent_gb300 as uw
+    threads = threads or max(1, min(16, (os.cpu_count() or 4)))
+
+    def one(r):
+        return uw.encode(r.weights(), uw.CODEC_HUFFMAN)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        return list(ex.map(one, recipes))
+
+
+def point_line(cfg, mat_desc, B, us, comp_bytes, eff_bytes, flops, plan, hbm, tf_peak, extra=None):
+    d = {"config": cfg, "matrix": mat_desc, "B": B, "us": round(us, 2),
+         "compressed_GBps": round(comp_bytes / us / 1e3, 1), "compressed_frac": round(comp_bytes / us / 1e3 / hbm, 3),
+         "effective_GBps": round(eff_bytes / us / 1e3, 1), "effective_frac": round(eff_bytes / us / 1e3 / hbm, 3),
+         "tflops": round(flops / us / 1e6, 1), "tensor_frac": round(flops / us / 1e6 / tf_peak, 3), "plan": plan}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def measure_workload(cfg, mat, batches, resident, stream, hbm, tf_peak, blob=None):
+    """Graph-timed, autotuned points of one matrix recipe: one line per batch size."""
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    blob = blob if blob is not None else uw.encode(mat.weights(), uw.CODEC_HUFFMAN)
+    single = mat.N * mat.K * 2 < L2_BYTES // 2
+    mats = [uw.Matrix(blob, resident=resident)] if single else load_copies(blob, resident)
+    copies = len(mats)
+    autotune_shared(mats, batches)
+    info = mats[0].info
+    out = []
+    for B in batches:
+        ws_bytes = max(m.workspace_size(B) for m in mats)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+        x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+        y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+        n = 32 if copies > 1 else 64
+        us = time_graph(lambda i, s: mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s),
+                        n, 7, stream) / n
+        plan = mats[0].plan_for(B)
+        strat = 4 if info["has_palette_form"] else 5
+        eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+        out.append(point_line(cfg, f"W[{mat.N},{mat.K}]", B, us, algorithmic_bytes(info, strat, B), eff,
+                              2.0 * B * mat.N * mat.K, plan.as_tuple(), hbm, tf_peak,
+                              {"kernel": kernel_name(plan, B), "resident": resident,
+                               "resident_ratio": round(info["device_bytes"] / (2 * mat.N * mat.K), 4),
+                               "l2": "matrix smaller than L2" if copies == 1 else
+                               f"{copies} copies rotated, inputs larger than L2",
+                               "verbatim_block_fraction": round(info["n_verbatim"] / info["n_blocks"], 4)}))
+        del ws, x, y
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_stack(layers, batches, stream, hbm, tf_peak, resident="palette"):
+    """The 8B MLP stack: gate, up, down per layer (per-layer seeds), one graph per pass over all 3 x layers
+    matmuls; the gate/up shape and the down shape are autotuned once each and the tables shared by shape."""
     import torch
 
     import lossless_bf16_weight_exponent_gb300 as uw
     import synth
-    hbm, tf_peak, peak_kind = peaks()
-    stream = torch.cuda.Stream()
-    single = [("tiny", synth.tiny(), [1]), ("gate_8b", synth.gate_8b(), [1, 4, 16]),
-              ("heavy_tail", synth.heavy_tail(), [1, 16, 64]),
-              ("gate_70b", synth.mlp_70b()[0], [1, 32, 256, 512]), ("down_70b", synth.mlp_70b()[2], [1, 32, 256, 512])]
-
-    def line(cfg, mat_desc, B, us, comp_bytes, eff_bytes, flops, plan, extra=None):
-        d = {"config": cfg, "matrix": mat_desc, "B": B, "us": round(us, 2),
-             "compressed_GBps": round(comp_bytes / us / 1e3, 1), "compressed_frac": round(comp_bytes / us / 1e3 / hbm, 3),
-             "effective_GBps": round(eff_bytes / us / 1e3, 1), "effective_frac": round(eff_bytes / us / 1e3 / hbm, 3),
-             "tflops": round(flops / us / 1e6, 1), "tensor_frac": round(flops / us / 1e6 / tf_peak, 3),
-             "plan": plan, "peak_kind": peak_kind}
-        if extra:
-            d.update(extra)
-        print(json.dumps(d), flush=True)
-
-    # the same matrices held as the Huffman blob alone (no palette form): the Huffman-fed pipelines
-    single += [("gate_8b/huffman", synth.gate_8b(), [1, 4, 8]), ("gate_70b/huffman", synth.mlp_70b()[0], [1, 8]),
-               ("down_70b/huffman", synth.mlp_70b()[2], [1])]
-    for cfg, mat, bs in single:
-        pal_form = not cfg.endswith("/huffman")
-        blob = uw.encode(mat.weights(), uw.CODEC_HUFFMAN)
-        base = uw.Matrix(blob, want_palette_form=pal_form)
-        info = base.info
-        copies = 1 if cfg == "tiny" else max(2, int(np.ceil(3 * L2_BYTES / info["device_bytes"])))
-        mats = [base] + [uw.Matrix(blob, want_palette_form=pal_form) for _ in range(copies - 1)]
-        need = base.autotune_workspace_size(bs)
-        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        base.autotune(bs, tws, need)
+    recipes = synth.stack_8b(layers)
+    blobs = encode_many(recipes)
+    mats = [uw.Matrix(b, resident=resident) for b in blobs]
+    del blobs
+    infos = [m.info for m in mats]
+    tables = {}
+    for first in (0, 2):
+        need = mats[first].autotune_workspace_size(batches)
+        tws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+        mats[first].autotune(batches, tws, need)
         del tws
-        table = base.tune_save()
-        for m in mats[1:]:
-            m.tune_load(table)
-        for B in bs:
-            ws_bytes = base.workspace_size(B)
-            ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-            x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
-            y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
-            n = 32 if copies > 1 else 64
-            us = time_graph(lambda i, s: mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s),
-                            n, 7, stream) / n
-            eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
-            line(cfg, f"W[{mat.N},{mat.K}]", B, us, algorithmic_bytes(info, 4 if pal_form else 5, B), eff,
-                 2.0 * B * mat.N * mat.K,
-                 base.plan_for(B).as_tuple(),
-                 {"l2": "matrix smaller than L2" if copies == 1 else f"{copies} copies rotated, inputs larger than L2",
-                  "verbatim_block_fraction": round(info["n_verbatim"] / info["n_blocks"], 4)})
-        del mats, base
-        torch.cuda.empty_cache()
-
-    # 8B MLP stack: gate, up, down per layer, one graph per pass over the whole stack
-    L = args.stack_layers
-    recipes = synth.stack_8b(L)
-    mats, infos, tables = [], [], {}
-    for r in recipes:
-        blob = uw.encode(r.weights(), uw.CODEC_HUFFMAN)
-        m = uw.Matrix(blob, want_palette_form=True)
-        mats.append(m)
-        infos.append(m.info)
-    bs = [1, 8, 32, 128]
-    for shape_first in (0, 2):  # autotune the gate shape and the down shape once, share by shape
-        m0 = mats[shape_first]
-        need = m0.autotune_workspace_size(bs)
-        tws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        m0.autotune(bs, tws, need)
-        del tws
-        tables[shape_first] = m0.tune_save()
+        tables[first] = mats[first].tune_save()
     for i, m in enumerate(mats):
         m.tune_load(tables[0 if i % 3 != 2 else 2])
-    for B in bs:
+    out = []
+    for B in batches:
         ws_bytes = max(m.workspace_size(B) for m in mats[:3])
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
         x_in = torch.from_numpy(recipes[0].activations(B).view(np.int16)).cuda()            # [B, 4096]
@@ -589,18 +492,321 @@ def run_sweep(args):
         y_out = torch.empty((B, 4096), dtype=torch.float32, device="cuda")
 
         def call(i, s):
-            m = mats[i]
             if i % 3 == 2:
-                m.matmul(x_mid, B, y_out, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+                mats[i].matmul(x_mid, B, y_out, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
             else:
-                m.matmul(x_in, B, y_mid, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+                mats[i].matmul(x_in, B, y_mid, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
         us = time_graph(call, len(mats), 5, stream)
-        comp = sum(algorithmic_bytes(inf, 4, B) for inf in infos)
+        strat = 4 if infos[0]["has_palette_form"] else 5
+        comp = sum(algorithmic_bytes(inf, strat, B) for inf in infos)
         eff = sum(2 * inf["N"] * inf["K"] + 2 * B * inf["K"] + 4 * B * inf["N"] for inf in infos)
         flops = sum(2.0 * B * inf["N"] * inf["K"] for inf in infos)
-        line("stack_8b", f"{L} layers x (gate, up W[14336,4096]; down W[4096,14336])", B, us, comp, eff, flops,
-             {"gate_up": mats[0].plan_for(B).as_tuple(), "down": mats[2].plan_for(B).as_tuple()},
-             {"matmuls": len(mats), "us_per_matmul": round(us / len(mats), 2)})
+        out.append(point_line("stack_8b", f"{layers} layers x (gate, up W[14336,4096]; down W[4096,14336])", B, us,
+                              comp, eff, flops,
+                              {"gate_up": mats[0].plan_for(B).as_tuple(), "down": mats[2].plan_for(B).as_tuple()},
+                              hbm, tf_peak,
+                              {"matmuls": len(mats), "us_per_matmul": round(us / len(mats), 2), "resident": resident,
+                               "resident_ratio": round(sum(i["device_bytes"] for i in infos) /
+                                                       sum(2 * i["N"] * i["K"] for i in infos), 4)}))
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
+def strategy_breakdown(blob, mat, info_both, hbm_peak):
+    """Per (B, strategy) timing of single eager calls rotating device copies that hold both the stream and the
+    palette form (every strategy available), L2 not warm."""
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    mats = load_copies(blob, "both")
+    copies = len(mats)
+    out = {}
+    names = {1: "full_decode", 2: "exp_only", 3: "palette_transcode", 4: "direct_palette", 5: "huffman_direct"}
+    for B in (1, 4, 16):
+        x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+        y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+        eff = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+        row = {}
+        for s, nm in names.items():
+            if s == 5 and B > 8:
+                continue  # the Huffman-direct GEMV takes B <= 8
+            need = mats[0].workspace_size(B, s)
+            ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+            for i in range(6):
+                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
+            st = torch.cuda.current_stream()
+            reps = 40
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+            for i in range(reps):
+                ev[2 * i].record(st)
+                mats[i % copies].matmul(x, B, y, uw.OUT_F32, s, ws, need)
+                ev[2 * i + 1].record(st)
+            torch.cuda.synchronize()
+            us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(reps))
+            alg = algorithmic_bytes(info_both, s, B)
+            row[nm] = {"us": round(us, 2), "eff_GBps": round(eff / us / 1e3, 1),
+                       "compressed_GBps": round(alg / us / 1e3, 1), "compressed_frac": round(alg / us / 1e3 / hbm_peak, 3)}
+        out[f"B={B}"] = row
+    del mats
+    torch.cuda.empty_cache()
+    return out
+
+
+def footprint(blob, N, K):
+    """Device bytes each resident form of the Huffman blob holds, against 2 N K bytes of BF16."""
+    import lossless_bf16_weight_exponent_gb300 as uw
+    out = {}
+    for r in ("huffman", "palette", "both"):
+        m = uw.Matrix(blob, resident=r)
+        out[r] = round(m.info["device_bytes"] / (2 * N * K), 4)
+        m.close()
+    return out
+
+
+def e2e_async(mats, mat, B, steps):
+    """End-to-end throughput through uw_matmul_host_async: every step copies its X from pinned host memory, runs the
+    matmul of the autotuned plan and copies Y back into pinned host memory; two streams alternate, each with its own
+    workspace and host buffers, so one step's copies overlap another's matmul.  Timed on the host clock from the
+    first call to both streams' completion."""
+    import torch
+    copies = len(mats)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    need = max(m.host_workspace_size(B) for m in mats)
+    wss = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in streams]
+    xh = [torch.from_numpy(mat.activations(B).view(np.int16)).pin_memory() for _ in streams]
+    yh = [torch.empty((B, mat.N), dtype=torch.float32).pin_memory() for _ in streams]
+
+    def run(n):
+        for i in range(n):
+            j = i & 1
+            mats[i % copies].matmul_host_async(xh[j], B, yh[j], 0, wss[j], need, streams[j])
+        for s in streams:
+            s.synchronize()
+    run(20)
+    t0 = time.perf_counter()
+    run(steps)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(blob, w, mat, B):
+    x = mat.activations(B)
+    times = oracle_step_seconds(blob, w.shape, x, 2)
+    sec = sum(times) / len(times)
+    eff = (2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N) / sec / 1e9
+    return {"value": eff, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"2 full steps: plain-C decode of the Huffman blob + fp64 GEMV at B={B}"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    import synth
+
+    rank, world, local = dist_setup()
+    dev = torch.cuda.current_device()
+    hbm_peak, tf_peak, tf_sust, peak_kind = peaks()
+    B = args.batch
+    mat = workload_matrix(args.workload)
+    w = mat.weights()
+    blob = uw.encode(w, uw.CODEC_HUFFMAN)
+    mats = load_copies(blob, args.resident)
+    base = mats[0]
+    info = base.info
+    resident_bytes = info["device_bytes"]
+    copies = len(mats)
+
+    # autotune on one copy (batches of the workload), share the table with the others
+    tune_batches = [1, 4, 16] if B in (1, 4, 16) else [B]
+    if args.plan:
+        vals = [int(v) for v in args.plan.split(",")]
+        text = "%d %d %d %d %d 0\n" % (1 << max(0, (B - 1).bit_length()), *vals)
+        for m in mats:
+            m.tune_load(text)
+    elif not args.no_autotune:
+        autotune_shared(mats, tune_batches)
+    plan = base.plan_for(B)
+    ws_bytes = max(m.workspace_size(B) for m in mats)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+    y = torch.empty((B, mat.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(i, s):
+        mats[i % copies].matmul(x, B, y, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
+
+    # CUDA graphs of G steps each, replayed to reach exactly n steps
+    K, W = args.steps, max(3, args.warmup)
+    G = min(64, K)
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(n):  # warm the plan outside capture once
+                    step(i, stream)
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(n):
+                        step(i, stream)
+            graphs[n] = g
+        return graphs[n]
+
+    def run_steps(n):
+        full, rem = divmod(n, G)
+        gf = graph_for(G) if full else None
+        gr = graph_for(rem) if rem else None
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                gf.replay()
+            if gr is not None:
+                gr.replay()
+
+    # every graph the warm-up and the timed region replay exists before timing starts
+    for n in {G, K % G, W % G, min(W, G)} - {0}:
+        graph_for(n)
+    # a first estimate of the step time, for the length of the clock ramp
+    t0 = time.perf_counter()
+    run_steps(G)
+    stream.synchronize()
+    est = max((time.perf_counter() - t0) / G, 1e-6)
+
+    clocks = Clocks(gpu_id(dev))
+    clocks.start()
+    run_steps(G * max(1, int(min(2e5, 0.5 / est) // G)))   # untimed load ramp: the sampled clocks see the GPU working
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    gate = StreamGate()
+    gated = gate.close(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        run_steps(W)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+        run_steps(K)
+        with torch.cuda.stream(stream):
+            e1.record(stream)
+    finally:
+        if gated:
+            gate.open()
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(e0.elapsed_time(e1), world)
+    ms_step = ms_total / K
+
+    alg = algorithmic_bytes(info, plan.strategy, B)
+    eff_bytes = 2 * mat.N * mat.K + 2 * B * mat.K + 4 * B * mat.N
+    value = job_throughput(eff_bytes, K, world, ms_total)
+    launches_per_step = launches_per_call(plan, B)
+
+    # e2e through the public API with host buffers: H2D of X and D2H of Y inside the timed region, every step
+    e2e_steps = min(max(K, 200), 4000)
+    e2e_s = max_over_ranks(e2e_async(mats, mat, B, e2e_steps), world)
+    e2e_value = job_throughput(eff_bytes, e2e_steps, world, e2e_s * 1e3)
+
+    forms = footprint(blob, mat.N, mat.K) if rank == 0 else None
+    breakdown, points = {}, []
+    if not args.no_breakdown and rank == 0 and args.workload == "gate_8b":
+        breakdown = strategy_breakdown(blob, mat, uw.Matrix(blob, resident="both").info, hbm_peak)
+        points = measure_points(args, stream, hbm_peak, tf_peak)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(blob, w, mat, B)
+
+    if rank == 0:
+        achieved = alg / (ms_step * 1e-3) / 1e9
+        kname = kernel_name(plan, B)
+        traffic, traffic_note = measured_traffic(args.workload, B, kname)
+        form = {"palette": "Huffman blob transcoded at load time into its palette form, the stream dropped",
+                "huffman": "Huffman blob alone", "both": "Huffman blob + its palette form"}[args.resident]
+        line = {
+            "metric": "effective BF16 weight GB/s, fused decompress+matmul (B=%d)" % B,
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_step, "us_per_matmul": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: W[{mat.N},{mat.K}] bf16 ({mat.name} recipe), {form}; "
+                                   f"X[{B},{mat.K}] N(0,1)",
+                       "batch": B, "plan": plan.as_tuple(), "copies_rotated": copies,
+                       "l2": f"inputs larger than L2: {copies} copies x {resident_bytes / 1e6:.1f} MB resident",
+                       "timing": "warm-up and timed steps queued behind a device-side gate, CUDA events on the "
+                                 "launching stream" + ("" if gated else " (gate unavailable: launched directly)"),
+                       "compression": {"huffman_bits_per_weight": 8 * info["blob_bytes"] / (mat.N * mat.K),
+                                       "verbatim_block_fraction": info["n_verbatim"] / info["n_blocks"]},
+                       "footprint": {"resident_bytes": resident_bytes, "bf16_bytes": 2 * mat.N * mat.K,
+                                     "resident_ratio": resident_bytes / (2 * mat.N * mat.K),
+                                     "ratio_by_form": forms}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic, "traffic_source": traffic_note,
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg, "kernel": kname},
+            "effective_frac_of_peak": value / world / hbm_peak,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * B * mat.K,
+                    "d2h_bytes_per_step": 4 * B * mat.N, "us_per_call": e2e_s / e2e_steps * 1e6, "steps": e2e_steps,
+                    "api": "uw_matmul_host_async on two alternating streams, pinned host X and Y"},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "breakdown": breakdown,
+            "points": points,
+        }
+        s = json.dumps(line)
+        print(s, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(s + "\n")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_points(args, stream, hbm, tf_peak):
+    """Graph-timed, autotuned points of the other workloads (each within the points budget): the 8B gate as the
+    Huffman stream alone, the heavy-tailed matrix, the 70B gate and down projections, the 96-matmul 8B stack."""
+    import synth
+    t_start = time.time()
+    m70 = synth.mlp_70b()
+    todo = [("gate_8b/huffman", synth.gate_8b(), [1, 4], "huffman"),
+            ("heavy_tail", synth.heavy_tail(), [1, 64], "palette"),
+            ("gate_70b", m70[0], [1, 32, 256, 512], "palette"),
+            ("down_70b", m70[2], [1, 32, 256, 512], "palette"),
+            ("stack_8b", None, [1], "palette")]
+    out = []
+    for cfg, mat, bs, resident in todo:
+        if time.time() - t_start > args.points_budget:
+            out.append({"config": cfg, "skipped": f"points budget of {args.points_budget:.0f} s spent"})
+            continue
+        if cfg == "stack_8b":
+            out += measure_stack(args.stack_layers, bs, stream, hbm, tf_peak)
+        else:
+            out += measure_workload(cfg, mat, bs, resident, stream, hbm, tf_peak)
+    return out
+
+
+def run_sweep(args):
+    """Every configuration of the workload list at each of its batch sizes, autotuned plan, graph replays over
+    enough resident copies that a pass streams from HBM (except the tiny matrix, smaller than L2)."""
+    import torch
+
+    import synth
+    hbm, tf_peak, _, _ = peaks()
+    stream = torch.cuda.Stream()
+    m70 = synth.mlp_70b()
+    single = [("tiny", synth.tiny(), [1], "palette"), ("gate_8b", synth.gate_8b(), [1, 4, 16], "palette"),
+              ("heavy_tail", synth.heavy_tail(), [1, 16, 64], "palette"),
+              ("gate_70b", m70[0], [1, 32, 256, 512], "palette"), ("down_70b", m70[2], [1, 32, 256, 512], "palette"),
+              ("gate_8b/huffman", synth.gate_8b(), [1, 4, 8], "huffman"),
+              ("gate_70b/huffman", m70[0], [1, 8], "huffman"), ("down_70b/huffman", m70[2], [1], "huffman")]
+    for cfg, mat, bs, resident in single:
+        for d in measure_workload(cfg, mat, bs, resident, stream, hbm, tf_peak):
+            print(json.dumps(d), flush=True)
+    for d in measure_stack(args.stack_layers, [1, 8, 32, 128], stream, hbm, tf_peak):
+        print(json.dumps(d), flush=True)
 
 
 def main():

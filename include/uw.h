@@ -93,6 +93,22 @@ typedef enum {
 
 typedef enum { UW_OUT_F32 = 0, UW_OUT_BF16 = 1 } uw_out_dtype;
 
+/*
+ * What uw_load keeps on the device for a Huffman blob (a palette blob always
+ * keeps its 4-bit codes and has no stream):
+ *   UW_RESIDENT_HUFFMAN  the Huffman stream alone (the smallest form; the
+ *                        Huffman-fed pipelines and HUFFMAN_DIRECT run on it)
+ *   UW_RESIDENT_BOTH     the stream and the 4-bit palette form
+ *   UW_RESIDENT_PALETTE  the 4-bit palette form alone: the stream is transcoded
+ *                        at load time (the post's direct-palette form) and then
+ *                        dropped, so PALETTE_TRANSCODE and HUFFMAN_DIRECT are not
+ *                        available
+ * Matching the post's results section, the choice trades footprint against
+ * speed: the stream is about 10.8 bits per weight on Gaussian weights, the
+ * palette form about 12.1.
+ */
+typedef enum { UW_RESIDENT_HUFFMAN = 0, UW_RESIDENT_BOTH = 1, UW_RESIDENT_PALETTE = 2 } uw_resident;
+
 /* Matmul kernel families. */
 typedef enum {
     UW_KERNEL_AUTO = 0,
@@ -140,6 +156,7 @@ typedef struct {
     uint64_t device_bytes;   /* device memory held by the uw_matrix */
     int32_t has_palette_form;/* 4-bit codes resident (DIRECT_PALETTE available) */
     int32_t chunk_weights, max_code_len;
+    int32_t has_huffman_stream; /* the Huffman stream is resident (PALETTE_TRANSCODE, HUFFMAN_DIRECT available) */
 } uw_info;
 
 typedef struct uw_matrix uw_matrix;
@@ -162,13 +179,15 @@ uw_status uw_encode(const uint16_t *w_host, int64_t N, int64_t K, const uw_encod
  * uw_load - validate a blob fully on the host (magic, version, sizes, section
  *   bounds and alignment, bitmap/prefix/verbatim consistency, code lengths and
  *   Kraft sum, chunk offsets) and copy it to device memory owned by the new
- *   uw_matrix.  want_palette_form != 0 on a Huffman blob also materialises the
- *   4-bit palette codes on the device (the post's load-time transcode for the
- *   direct-palette pipeline).  Blocks the host until the upload on `stream` is
- *   done, so the caller may free `blob` on return.
- *   Errors: UW_ERR_CORRUPT (validation), UW_ERR_NO_MEMORY, UW_ERR_CUDA.
+ *   uw_matrix.  `resident` (uw_resident) says what stays on the device for a
+ *   Huffman blob; any form with the palette codes runs the post's load-time
+ *   transcode of the stream into 4-bit codes.  Blocks the host until the
+ *   upload on `stream` is done, so the caller may free `blob` on return.
+ *   uw_get_info reports the device bytes the matrix holds.
+ *   Errors: UW_ERR_INVALID_ARG (resident out of range), UW_ERR_CORRUPT
+ *   (validation), UW_ERR_NO_MEMORY, UW_ERR_CUDA.
  */
-uw_status uw_load(const void *blob, size_t size, int want_palette_form, uw_stream stream, uw_matrix **out);
+uw_status uw_load(const void *blob, size_t size, int resident, uw_stream stream, uw_matrix **out);
 
 /*
  * uw_blob_validate - the host-side checks of uw_load without any device work
@@ -236,6 +255,18 @@ uw_status uw_plan_for(const uw_matrix *m, int64_t B, uw_plan *out);
 uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
                          uw_out_dtype out_dtype, void *workspace, size_t ws_bytes, uw_stream stream);
 uw_status uw_host_workspace_size(const uw_matrix *m, int64_t B, uw_out_dtype out_dtype, size_t *bytes);
+
+/*
+ * uw_matmul_host_async - uw_matmul_host without the final synchronisation: the
+ *   copy of X, the matmul and the copy of Y back are enqueued on `stream` and
+ *   the call returns.  x_host must stay unchanged, and y_host unread, until
+ *   the stream has passed the copy back (synchronise the stream or an event
+ *   recorded after the call); the workspace belongs to the call until then.
+ *   With pinned host buffers and two streams, one call's copies overlap the
+ *   other's matmul.  Errors as uw_matmul_host.
+ */
+uw_status uw_matmul_host_async(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
+                               uw_out_dtype out_dtype, void *workspace, size_t ws_bytes, uw_stream stream);
 
 /*
  * uw_matmul_noalloc - uw_matmul with the palette-transcode pipeline

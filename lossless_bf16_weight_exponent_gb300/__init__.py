@@ -27,6 +27,8 @@ STRAT_HUFFMAN_DIRECT = 5
 STRATEGIES = {"full_decode": 1, "exp_only": 2, "palette_transcode": 3, "direct_palette": 4, "huffman_direct": 5}
 OUT_F32, OUT_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_TC = 0, 1, 2
+RESIDENT_HUFFMAN, RESIDENT_BOTH, RESIDENT_PALETTE = 0, 1, 2
+RESIDENT = {"huffman": RESIDENT_HUFFMAN, "both": RESIDENT_BOTH, "palette": RESIDENT_PALETTE}
 
 
 class UwError(RuntimeError):
@@ -57,7 +59,7 @@ class Info(ctypes.Structure):
                 ("n_blocks", ctypes.c_uint64), ("n_verbatim", ctypes.c_uint64), ("n_chunks", ctypes.c_uint64),
                 ("total_bits", ctypes.c_uint64), ("blob_bytes", ctypes.c_uint64), ("device_bytes", ctypes.c_uint64),
                 ("has_palette_form", ctypes.c_int32), ("chunk_weights", ctypes.c_int32),
-                ("max_code_len", ctypes.c_int32)]
+                ("max_code_len", ctypes.c_int32), ("has_huffman_stream", ctypes.c_int32)]
 
     def as_dict(self):
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -82,6 +84,7 @@ _SIGS = {
     "uw_plan_workspace_size": [_VP, _I64, ctypes.POINTER(Plan), ctypes.POINTER(_SZ)],
     "uw_plan_for": [_VP, _I64, ctypes.POINTER(Plan)],
     "uw_matmul_host": [_VP, _VP, _I64, _VP, _INT, _VP, _SZ, _VP],
+    "uw_matmul_host_async": [_VP, _VP, _I64, _VP, _INT, _VP, _SZ, _VP],
     "uw_host_workspace_size": [_VP, _I64, _INT, ctypes.POINTER(_SZ)],
     "uw_autotune": [_VP, ctypes.POINTER(_I64), _INT, _VP, _SZ, _VP],
     "uw_autotune_workspace_size": [_VP, ctypes.POINTER(_I64), _INT, ctypes.POINTER(_SZ)],
@@ -166,11 +169,13 @@ def validate(blob: bytes) -> dict:
 class Matrix:
     """A compressed matrix resident on the current CUDA device (owns a ``uw_matrix``)."""
 
-    def __init__(self, blob: bytes, want_palette_form: bool = False, stream=None):
+    def __init__(self, blob: bytes, want_palette_form: bool = False, stream=None, resident=None):
+        """resident: "huffman", "both" or "palette" (uw_resident); if None, want_palette_form picks "both" (True)
+        or "huffman" (False)."""
+        mode = RESIDENT[resident] if resident is not None else (RESIDENT_BOTH if want_palette_form else RESIDENT_HUFFMAN)
         buf = np.frombuffer(blob, np.uint8)
         h = ctypes.c_void_p()
-        _check(lib().uw_load(buf.ctypes.data, len(blob), int(want_palette_form), _stream(stream), ctypes.byref(h)),
-               "uw_load")
+        _check(lib().uw_load(buf.ctypes.data, len(blob), mode, _stream(stream), ctypes.byref(h)), "uw_load")
         self._h = h
         info = Info()
         _check(lib().uw_get_info(self._h, ctypes.byref(info)), "uw_get_info")
@@ -228,6 +233,10 @@ class Matrix:
     def matmul_host(self, x_host, B: int, y_host, out_dtype: int, workspace, ws_bytes: int, stream=None):
         _check(lib().uw_matmul_host(self._h, _ptr(x_host), B, _ptr(y_host), out_dtype, _ptr(workspace), ws_bytes,
                                     _stream(stream)), "uw_matmul_host")
+
+    def matmul_host_async(self, x_host, B: int, y_host, out_dtype: int, workspace, ws_bytes: int, stream=None):
+        _check(lib().uw_matmul_host_async(self._h, _ptr(x_host), B, _ptr(y_host), out_dtype, _ptr(workspace),
+                                          ws_bytes, _stream(stream)), "uw_matmul_host_async")
 
     def autotune_workspace_size(self, batches) -> int:
         arr = (ctypes.c_int64 * len(batches))(*batches)

@@ -802,7 +802,8 @@ bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaSha
 bool gemv_tma_supported(const WOperand &w, int64_t B, int variant)
 {
     TmaShape s;
-    return variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
+    // the verbatim pass of 4-bit-code stages reads the verbatim records, built when codes are resident
+    return (w.fmt != FMT_PAL || w.verb_rec) && variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
            plan_variant(w, B, 0, variant, s);
 }
 
@@ -810,7 +811,7 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
                     float *acc_ws, int *status, void *stream)
 {
     TmaShape s;
-    if (!plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
+    if ((w.fmt == FMT_PAL && !w.verb_rec) || !plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
     const int nb = B <= 1 ? 1 : 2;
     cudaStream_t st = (cudaStream_t)stream;
     TmaArgs a;

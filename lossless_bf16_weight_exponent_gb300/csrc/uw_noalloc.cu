@@ -94,8 +94,9 @@ extern "C" uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev
     uw_info info;
     uw_status s = uw_get_info(m, &info);
     if (s != UW_OK) return s;
-    if (info.codec != UW_CODEC_HUFFMAN)
-        return uw::fail(UW_ERR_UNSUPPORTED, "uw_matmul_noalloc: needs a Huffman-coded matrix (palette transcode)");
+    if (info.codec != UW_CODEC_HUFFMAN || !info.has_huffman_stream)
+        return uw::fail(UW_ERR_UNSUPPORTED,
+                        "uw_matmul_noalloc: needs a Huffman-coded matrix with its stream resident (palette transcode)");
     if (B < 0) return uw::fail(UW_ERR_SHAPE, "uw_matmul_noalloc: B < 0");
     if (B == 0 || info.N == 0) return UW_OK;
     if (!x_dev || !y_dev || ((uintptr_t)x_dev & 15) || ((uintptr_t)y_dev & 15))

@@ -47,6 +47,7 @@ struct uw_matrix {
     const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
     const uint8_t *tmv_data = nullptr;
     const uint8_t *verb_rec = nullptr;
+    bool has_stream = false;  // the Huffman stream (offsets, bits, tables) is resident
     int device = 0;
     std::mutex mu;
     std::vector<TuneEntry> tune;
@@ -84,17 +85,25 @@ static uw_status cuda_fail(cudaError_t e, const char *what)
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // ------------------------------------------------------------------------------ load / free
-extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_form, uw_stream stream, uw_matrix **out)
+extern "C" uw_status uw_load(const void *blob, size_t size, int resident, uw_stream stream, uw_matrix **out)
 {
     clear_error();
     if (!out) return fail(UW_ERR_INVALID_ARG, "uw_load: out is NULL");
     *out = nullptr;
+    if (resident < UW_RESIDENT_HUFFMAN || resident > UW_RESIDENT_PALETTE)
+        return fail(UW_ERR_INVALID_ARG, "uw_load: resident %d out of range", resident);
     BlobHeader h;
     uw_status s = parse_and_validate((const uint8_t *)blob, size, &h, true);
     if (s != UW_OK) return s;
     const uint8_t *p = (const uint8_t *)blob;
     const uint64_t n = (uint64_t)h.N * (uint64_t)h.K;
-    const bool resident_codes = h.codec == UW_CODEC_PALETTE || want_palette_form;
+    const bool huff = h.codec == UW_CODEC_HUFFMAN;
+    // what stays resident: the 4-bit codes (a palette blob always; a Huffman blob unless only its stream is
+    // wanted) and the Huffman stream with its offsets and tables (a Huffman blob unless only the codes are)
+    const bool resident_codes = !huff || resident != UW_RESIDENT_HUFFMAN;
+    const bool resident_stream = huff && resident != UW_RESIDENT_PALETTE;
+    const bool multi = huff && h.max_len <= 12;
+    const uint64_t tab_bytes = huff ? ((uint64_t)1 << h.max_len) : 16;
 
     // device layout: every piece 256-aligned, streams padded so vector loads may run past the end
     uint64_t off = 0;
@@ -104,14 +113,19 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     const uint64_t o_pf = take(h.len[S_PREFIX] + 16);
     const uint64_t o_ve = take(h.len[S_VERB] + 16);
     const uint64_t o_codes = resident_codes ? take(n / 2 + 64) : 0;
-    const uint64_t o_co = take(h.len[S_CHUNK] + 16);
-    const uint64_t o_bits = take(h.len[S_BITS] + 512);
-    const uint64_t tab_bytes = h.codec == UW_CODEC_HUFFMAN ? ((uint64_t)1 << h.max_len) : 16;
-    const uint64_t o_tab = take(tab_bytes);
-    const bool multi = h.codec == UW_CODEC_HUFFMAN && h.max_len <= 12;
-    const uint64_t o_mtab = multi ? take(4096 * 4) : 0;
+    // the Huffman stream: in the matrix's own memory when it stays resident, else in a load-time buffer that
+    // only feeds the transcode into the codes
+    uint64_t hoff = 0;
+    auto take_h = [&](uint64_t bytes) {
+        if (resident_stream) return take(bytes);
+        uint64_t o = hoff; hoff = round_up(hoff + bytes, 256); return o;
+    };
+    const uint64_t o_co = huff ? take_h(h.len[S_CHUNK] + 16) : 0;
+    const uint64_t o_bits = huff ? take_h(h.len[S_BITS] + 512) : 0;
+    const uint64_t o_tab = huff ? take_h(tab_bytes) : 0;
+    const uint64_t o_mtab = multi ? take_h(4096 * 4) : 0;
     const uint64_t o_st = take(256);
-    // tile-major verbatim stream for the tcgen05 kernels (units of 128 rows x 256 weights)
+    // tile-major verbatim stream for the unit-walking kernels (units of 128 rows x 256 weights)
     std::vector<uint32_t> tmv_off, tmv_mask;
     std::vector<uint8_t> tmv_data;
     const bool tmv = h.K % 256 == 0 && h.N > 0;
@@ -119,10 +133,11 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     const uint64_t o_tmo = tmv ? take(tmv_off.size() * 4 + 16) : 0;
     const uint64_t o_tmm = tmv ? take(tmv_mask.size() * 4 + 16) : 0;
     const uint64_t o_tmd = tmv ? take(tmv_data.size() + 64) : 0;
-    // verbatim records (exponents + sign+mantissa bytes per verbatim block) for the GEMV's verbatim pass
+    // verbatim records (exponents + sign+mantissa bytes per verbatim block) for the bulk-copy GEMV's verbatim
+    // pass, which reads 4-bit codes: built when codes are resident
     std::vector<uint8_t> vrec;
-    build_verbatim_records(h, p, vrec);
-    const uint64_t o_vr = take(vrec.size() + 64);
+    if (resident_codes) build_verbatim_records(h, p, vrec);
+    const uint64_t o_vr = resident_codes ? take(vrec.size() + 64) : 0;
 
     uw_matrix *m = new (std::nothrow) uw_matrix();
     if (!m) return fail(UW_ERR_NO_MEMORY, "uw_load: host allocation");
@@ -132,16 +147,26 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     if (e != cudaSuccess) { delete m; return fail(UW_ERR_NO_MEMORY, "uw_load: cudaMalloc(%llu): %s", (unsigned long long)off, cudaGetErrorString(e)); }
     m->dev_bytes = off;
     uint8_t *d = (uint8_t *)m->dev;
+    uint8_t *hd = d;  // base of the Huffman pieces
+    if (huff && !resident_stream) {
+        if ((e = cudaMalloc(&hd, hoff)) != cudaSuccess) {
+            cudaFree(m->dev); delete m;
+            return fail(UW_ERR_NO_MEMORY, "uw_load: cudaMalloc(%llu): %s", (unsigned long long)hoff, cudaGetErrorString(e));
+        }
+    }
     cudaStream_t st = (cudaStream_t)stream;
-    auto fail_free = [&](uw_status code) { cudaFree(m->dev); delete m; return code; };
-    if ((e = cudaMemsetAsync(d, 0, off, st)) != cudaSuccess) return fail_free(cuda_fail(e, "uw_load: memset"));
-    auto up = [&](uint64_t dst, int sec) -> cudaError_t {
-        if (!h.len[sec]) return cudaSuccess;
-        return cudaMemcpyAsync(d + dst, p + h.off[sec], h.len[sec], cudaMemcpyHostToDevice, st);
+    auto fail_free = [&](uw_status code) {
+        if (hd != d) cudaFree(hd);
+        cudaFree(m->dev); delete m; return code;
     };
-    if ((e = up(o_sm, S_SM)) || (e = up(o_bm, S_BITMAP)) || (e = up(o_pf, S_PREFIX)) || (e = up(o_ve, S_VERB)) ||
-        (resident_codes && h.codec == UW_CODEC_PALETTE && (e = up(o_codes, S_IDX))) || (e = up(o_co, S_CHUNK)) ||
-        (e = up(o_bits, S_BITS)))
+    if ((e = cudaMemsetAsync(d, 0, off, st)) != cudaSuccess) return fail_free(cuda_fail(e, "uw_load: memset"));
+    if (hd != d && (e = cudaMemsetAsync(hd, 0, hoff, st)) != cudaSuccess) return fail_free(cuda_fail(e, "uw_load: memset"));
+    auto up = [&](uint8_t *base, uint64_t dst, int sec) -> cudaError_t {
+        if (!h.len[sec]) return cudaSuccess;
+        return cudaMemcpyAsync(base + dst, p + h.off[sec], h.len[sec], cudaMemcpyHostToDevice, st);
+    };
+    if ((e = up(d, o_sm, S_SM)) || (e = up(d, o_bm, S_BITMAP)) || (e = up(d, o_pf, S_PREFIX)) || (e = up(d, o_ve, S_VERB)) ||
+        (!huff && (e = up(d, o_codes, S_IDX))) || (huff && ((e = up(hd, o_co, S_CHUNK)) || (e = up(hd, o_bits, S_BITS)))))
         return fail_free(cuda_fail(e, "uw_load: upload"));
     if (tmv && ((e = cudaMemcpyAsync(d + o_tmo, tmv_off.data(), tmv_off.size() * 4, cudaMemcpyHostToDevice, st)) ||
                 (e = cudaMemcpyAsync(d + o_tmm, tmv_mask.data(), tmv_mask.size() * 4, cudaMemcpyHostToDevice, st)) ||
@@ -152,13 +177,13 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
         return fail_free(cuda_fail(e, "uw_load: verbatim record upload"));
     std::vector<uint8_t> table;
     std::vector<uint32_t> mtable;
-    if (h.codec == UW_CODEC_HUFFMAN) {
+    if (huff) {
         build_decode_table(h.code_len, (int)h.max_len, table);
-        if ((e = cudaMemcpyAsync(d + o_tab, table.data(), table.size(), cudaMemcpyHostToDevice, st)))
+        if ((e = cudaMemcpyAsync(hd + o_tab, table.data(), table.size(), cudaMemcpyHostToDevice, st)))
             return fail_free(cuda_fail(e, "uw_load: table upload"));
         if (multi) {
             build_multi_table(h.code_len, mtable);
-            if ((e = cudaMemcpyAsync(d + o_mtab, mtable.data(), mtable.size() * 4, cudaMemcpyHostToDevice, st)))
+            if ((e = cudaMemcpyAsync(hd + o_mtab, mtable.data(), mtable.size() * 4, cudaMemcpyHostToDevice, st)))
                 return fail_free(cuda_fail(e, "uw_load: table upload"));
         }
     }
@@ -173,16 +198,20 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     v.verb_exp = d + o_ve;
     m->codes = resident_codes ? d + o_codes : nullptr;
     v.codes = m->codes;
-    v.chunk_off = (const uint32_t *)(d + o_co);
-    v.bits = (const uint32_t *)(d + o_bits);
-    v.dtab = d + o_tab;
-    v.mtab = multi ? (const uint32_t *)(d + o_mtab) : nullptr;
+    if (huff) {
+        v.chunk_off = (const uint32_t *)(hd + o_co);
+        v.bits = (const uint32_t *)(hd + o_bits);
+        v.dtab = hd + o_tab;
+        v.mtab = multi ? (const uint32_t *)(hd + o_mtab) : nullptr;
+    }
     v.status = (int *)(d + o_st);
     m->tmv_off = tmv ? (const uint32_t *)(d + o_tmo) : nullptr;
     m->tmv_mask = tmv ? (const uint32_t *)(d + o_tmm) : nullptr;
     m->tmv_data = tmv ? d + o_tmd : nullptr;
-    m->verb_rec = d + o_vr;
-    if (h.codec == UW_CODEC_HUFFMAN && want_palette_form) {
+    m->verb_rec = resident_codes ? d + o_vr : nullptr;
+    m->has_stream = resident_stream;
+    if (huff && resident_codes) {
+        // the post's load-time transcode of the Huffman stream into the direct-palette form
         if ((e = (cudaError_t)launch_decode_huffman(v, DEC_CODES, m->codes, st)))
             return fail_free(cuda_fail(e, "uw_load: palette transcode"));
     }
@@ -191,6 +220,14 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int want_palette_for
     if ((e = cudaMemcpy(&dev_status, v.status, sizeof(int), cudaMemcpyDeviceToHost)))
         return fail_free(cuda_fail(e, "uw_load: status read"));
     if (dev_status) return fail_free(fail(UW_ERR_CORRUPT, "uw_load: Huffman stream failed to decode"));
+    if (hd != d) {
+        // only the codes stay: the stream, its offsets and tables are gone
+        cudaFree(hd);
+        v.chunk_off = nullptr;
+        v.bits = nullptr;
+        v.dtab = nullptr;
+        v.mtab = nullptr;
+    }
     *out = m;
     return UW_OK;
 }
@@ -216,6 +253,7 @@ extern "C" uw_status uw_get_info(const uw_matrix *m, uw_info *out)
     out->total_bits = h.total_bits; out->blob_bytes = h.blob_bytes;
     out->device_bytes = m->dev_bytes;
     out->has_palette_form = m->codes != nullptr;
+    out->has_huffman_stream = m->has_stream;
     out->chunk_weights = (int32_t)h.chunk; out->max_code_len = (int32_t)h.max_len;
     return UW_OK;
 }
@@ -244,7 +282,8 @@ extern "C" uw_status uw_decode(const uw_matrix *m, uint16_t *w_dev, uw_stream st
     if (!n) return UW_OK;
     if (!w_dev || !aligned16(w_dev)) return fail(UW_ERR_INVALID_ARG, "uw_decode: output NULL or not 16-byte aligned");
     int e;
-    if (m->h.codec == UW_CODEC_PALETTE) e = launch_decode_palette(m->v, DEC_BF16, w_dev, stream);
+    // from the resident codes when there are any (a streaming decode), else from the Huffman stream
+    if (m->codes) e = launch_decode_palette(m->v, DEC_BF16, w_dev, stream);
     else e = launch_decode_huffman(m->v, DEC_BF16, w_dev, stream);
     if (e) return cuda_fail((cudaError_t)e, "uw_decode: launch");
     return UW_OK;
@@ -256,9 +295,9 @@ static bool strategy_ok(const uw_matrix *m, int s)
     switch (s) {
     case UW_STRAT_FULL_DECODE:
     case UW_STRAT_EXP_ONLY: return true;
-    case UW_STRAT_PALETTE_TRANSCODE: return m->h.codec == UW_CODEC_HUFFMAN;
+    case UW_STRAT_PALETTE_TRANSCODE: return m->has_stream;
     case UW_STRAT_DIRECT_PALETTE: return m->codes != nullptr;
-    case UW_STRAT_HUFFMAN_DIRECT: return m->h.codec == UW_CODEC_HUFFMAN && gemv_huff_supported(m->v, 1);
+    case UW_STRAT_HUFFMAN_DIRECT: return m->has_stream && gemv_huff_supported(m->v, 1);
     default: return false;
     }
 }
@@ -357,7 +396,7 @@ static uw_plan default_plan(const uw_matrix *m, int64_t B)
 {
     if (m->codes) return default_plan_for_strategy(m, B, UW_STRAT_DIRECT_PALETTE);
     // a Huffman matrix without its palette form: decode in the GEMV where it applies, else transcode first
-    if (m->h.codec == UW_CODEC_HUFFMAN && gemv_huff_supported(m->v, B))
+    if (m->has_stream && gemv_huff_supported(m->v, B))
         return default_plan_for_strategy(m, B, UW_STRAT_HUFFMAN_DIRECT);
     return default_plan_for_strategy(m, B, UW_STRAT_PALETTE_TRANSCODE);
 }
@@ -449,14 +488,12 @@ extern "C" uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x, int64
     int e = 0;
     switch (plan->strategy) {
     case UW_STRAT_FULL_DECODE:
-        e = m->h.codec == UW_CODEC_PALETTE ? launch_decode_palette(m->v, DEC_BF16, wsp, stream)
-                                           : launch_decode_huffman(m->v, DEC_BF16, wsp, stream);
+        e = m->codes ? launch_decode_palette(m->v, DEC_BF16, wsp, stream) : launch_decode_huffman(m->v, DEC_BF16, wsp, stream);
         w.w = (const uint16_t *)wsp;
         w.w_from_prev = 1;
         break;
     case UW_STRAT_EXP_ONLY:
-        e = m->h.codec == UW_CODEC_PALETTE ? launch_decode_palette(m->v, DEC_EXP, wsp, stream)
-                                           : launch_decode_huffman(m->v, DEC_EXP, wsp, stream);
+        e = m->codes ? launch_decode_palette(m->v, DEC_EXP, wsp, stream) : launch_decode_huffman(m->v, DEC_EXP, wsp, stream);
         w.exps = wsp;
         w.w_from_prev = 1;
         break;
@@ -509,8 +546,8 @@ extern "C" uw_status uw_host_workspace_size(const uw_matrix *m, int64_t B, uw_ou
     return UW_OK;
 }
 
-extern "C" uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
-                                    uw_out_dtype od, void *ws, size_t ws_bytes, uw_stream stream)
+extern "C" uw_status uw_matmul_host_async(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
+                                          uw_out_dtype od, void *ws, size_t ws_bytes, uw_stream stream)
 {
     clear_error();
     if (!m) return fail(UW_ERR_INVALID_ARG, "uw_matmul_host: NULL matrix");
@@ -530,7 +567,15 @@ extern "C" uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, 
     s = uw_matmul(m, (const uint16_t *)xd, B, yd, od, UW_STRAT_AUTO, p, round_up(inner, 256), stream);
     if (s != UW_OK) return s;
     UW_CUDA(cudaMemcpyAsync(y_host, yd, yb, cudaMemcpyDeviceToHost, st), "uw_matmul_host: D2H");
-    UW_CUDA(cudaStreamSynchronize(st), "uw_matmul_host: synchronize");
+    return UW_OK;
+}
+
+extern "C" uw_status uw_matmul_host(const uw_matrix *m, const uint16_t *x_host, int64_t B, void *y_host,
+                                    uw_out_dtype od, void *ws, size_t ws_bytes, uw_stream stream)
+{
+    uw_status s = uw_matmul_host_async(m, x_host, B, y_host, od, ws, ws_bytes, stream);
+    if (s != UW_OK) return s;
+    UW_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "uw_matmul_host: synchronize");
     return UW_OK;
 }
 

@@ -170,3 +170,12 @@ def test_matmul_host_end_to_end():
     ws = dev_bytes(need)
     m.matmul_host(xh, B, yh, uw.OUT_F32, ws, need)
     assert tol_ok(yh.numpy().astype(np.float64), yref, absum)[0]
+    # the asynchronous form on two streams, each call with its own buffers; results read after a synchronise
+    streams = [t.cuda.Stream(), t.cuda.Stream()]
+    wss = [dev_bytes(need), dev_bytes(need)]
+    ys = [t.full((B, mat.N), float("nan"), dtype=t.float32).pin_memory() for _ in range(4)]
+    for i in range(4):
+        m.matmul_host_async(xh, B, ys[i], uw.OUT_F32, wss[i % 2], need, streams[i % 2])
+    t.cuda.synchronize()
+    for i in range(4):
+        assert tol_ok(ys[i].numpy().astype(np.float64), yref, absum)[0], i

@@ -56,7 +56,7 @@ def run_matmul(m, x_np, plan_or_strategy, out_dtype=uw.OUT_F32, stream=None):
 
 def strategies_for(m):
     out = [uw.STRAT_FULL_DECODE, uw.STRAT_EXP_ONLY]
-    if m.info["codec"] == uw.CODEC_HUFFMAN:
+    if m.info["has_huffman_stream"]:
         out.append(uw.STRAT_PALETTE_TRANSCODE)
     if m.info["has_palette_form"]:
         out.append(uw.STRAT_DIRECT_PALETTE)
