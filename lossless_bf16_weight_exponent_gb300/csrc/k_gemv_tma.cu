@@ -18,13 +18,11 @@
 // free.  A consumer copies its part of a stage into registers and releases the
 // slot before computing on it.  Two 4-bit codes (one code byte) select the
 // exponent fields of a bf16x2 pair from a 32 KB per-lane table in shared memory,
-// so a warp's lookups never share a bank.  A stage without verbatim blocks runs a
-// straight-line body; a verbatim block's codes are all zero, so reading a zero table
-// row under a zero sign+mantissa mask, with its activations masked to zero as well,
-// makes it add exactly +0 * +0 (even for an infinite activation), and after the main
-// loop the consumers add the CTA's verbatim blocks' true products from records staged
-// in shared memory and X written into the freed ring - no warp runs a slower body that
-// would hold the ring back.  Lane sums of four consecutive stages
+// so a warp's lookups never share a bank.  A stage without verbatim blocks in the
+// warp runs a straight-line body; otherwise a lane whose 16 weights lie in a
+// verbatim block rebuilds them from that block's exponents, which the producer
+// stages (the CTA's contiguous run of them) with one bulk copy before the ring
+// fills.  Lane sums of four consecutive stages
 // are reduced together (a transposed butterfly), and row sums meet in shared
 // memory and are written once at the end.  A warp hands a slot back only after a
 // cross-proxy fence on its reads (the next bulk copy writes it through the async
@@ -69,7 +67,7 @@ struct TmaArgs {  // 64-byte aligned through its tensor maps
     int rows_cta;    // max rows owned by one CTA
     int bm_words;    // max verbatim-bitmap words of one CTA's rows
     int w_from_prev; // the weight stream is written by the preceding kernel (a preprocess workspace)
-    int vcap;        // verbatim records of the CTA staged in shared memory (beyond: global loads)
+    int vcap;        // verbatim blocks of the CTA whose exponents are staged in shared memory (beyond: global loads)
     int *status;
 };
 
@@ -264,14 +262,13 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     uint64_t *full = (uint64_t *)(smem + TB);                                 // [stages]
     uint64_t *empty = full + a.stages;                                        // [stages]
     uint64_t *vfull = empty + a.stages;                                       // staged verbatim records landed
-    uint8_t *zrow = smem + TB + 512;                                          // [128] zeros: verbatim groups' table row
     float *part = (float *)(smem + TB + 1024);                                // [rows_cta][NB]
     const int part_bytes = (a.rows_cta * NB * 4 + 1023) / 1024 * 1024;
     const int bm_bytes = (a.bm_words * 4 + 1023) / 1024 * 1024;
     uint32_t *bm = (uint32_t *)(smem + TB + 1024 + part_bytes);              // [bm_words] bitmap
     uint32_t *pf = (uint32_t *)(smem + TB + 1024 + part_bytes + bm_bytes);   // [bm_words] prefix
     uint8_t *ring = smem + TB + 1024 + part_bytes + 2 * bm_bytes;            // 1024-aligned: tensor copies want 128
-    uint8_t *vx = ring + (size_t)a.stages * a.stage_bytes;                    // [vcap][kVerbRec] verbatim records
+    uint8_t *vx = ring + (size_t)a.stages * a.stage_bytes;                    // [vcap][64] verbatim exponents
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = a.rs * a.wk;  // consumer warps
@@ -302,29 +299,25 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         const uint64_t pol_w = l2_evict_first();
         int issued = 0;
         bool ok = true;
-        bool verb_issued = FMT != FMT_PAL;
+        if (FMT == FMT_PAL && lane == 0) {
+            // first of all, the exponents of the CTA's verbatim blocks: ranks [v_begin, v_end) of the verbatim
+            // stream are one contiguous run (the CTA's rows are), of which the first vcap blocks are staged
+            uint32_t v_staged = 0;
+            uint64_t v_begin = 0;
+            if (nrows) {
+                const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
+                const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
+                const uint32_t bw0 = __ldg(a.w.bitmap + (fb >> 5)), pw0 = __ldg(a.w.prefix + (fb >> 5));
+                const uint32_t bw1 = __ldg(a.w.bitmap + lwd), pw1 = __ldg(a.w.prefix + lwd);
+                v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
+                const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
+                v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+            }
+            mbar_arrive_expect_tx(vfull, v_staged * 64);
+            if (v_staged) bulk_g2s_hint(vx, a.w.verb_exp + v_begin * 64, v_staged * 64, vfull, pol_w);
+        }
         for (int i = 0; i < n_stages; i++) {
             const int slot = i % a.stages;
-            if (!verb_issued && (i == a.stages || i + 1 == n_stages)) {
-                // the ring is primed: stage the CTA's verbatim records (ranks [v_begin, v_end) of the verbatim
-                // stream, at most vcap of them) for the verbatim pass after the main loop
-                if (lane == 0) {
-                    uint32_t v_staged = 0;
-                    uint64_t v_begin = 0;
-                    if (nrows) {
-                        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
-                        const uint64_t lwd = (lb & 31) ? lb >> 5 : (lb - 1) >> 5;
-                        const uint32_t bw0 = __ldg(a.w.bitmap + (fb >> 5)), pw0 = __ldg(a.w.prefix + (fb >> 5));
-                        const uint32_t bw1 = __ldg(a.w.bitmap + lwd), pw1 = __ldg(a.w.prefix + lwd);
-                        v_begin = pw0 + __popc(bw0 & ((1u << (fb & 31)) - 1u));
-                        const uint64_t v_end = (lb & 31) ? pw1 + __popc(bw1 & ((1u << (lb & 31)) - 1u)) : pw1 + __popc(bw1);
-                        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
-                    }
-                    mbar_arrive_expect_tx(vfull, v_staged * kVerbRec);
-                    if (v_staged) bulk_g2s_hint(vx, a.w.verb_rec + v_begin * kVerbRec, v_staged * kVerbRec, vfull, pol_w);
-                }
-                verb_issued = true;
-            }
             const int64_t g0 = r0 + (int64_t)i * a.rs;
             const int nr = (int)min((int64_t)a.rs, r1 - g0);
             const bool whole = a.tmap && nr == a.rs && klen == a.ks;  // one tensor copy per stream: the whole stage
@@ -359,11 +352,8 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             issued = i + 1;
         }
         if (lane == 0) {
-            if (FMT == FMT_PAL) {
-                if (!verb_issued) mbar_arrive_expect_tx(vfull, 0);  // no stages (or a timeout before priming)
-                // the staged records must land before the CTA may exit
-                if (!mbar_wait(vfull, 0)) ok = false;
-            }
+            // the staged verbatim exponents must land before the CTA may exit
+            if (FMT == FMT_PAL && !mbar_wait(vfull, 0)) ok = false;
             if (!ok) {
                 atomicExch(a.status, (int)DEV_TIMEOUT);
                 // drain: every issued stage's copies must land before the CTA may exit
@@ -381,7 +371,6 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
             pf[i] = i < n_bw ? __ldg(a.w.prefix + wb0 + i) : 0u;
         }
     for (int i = ctid; i < a.rows_cta * NB; i += CT) part[i] = 0.f;
-    if (ctid < 32) ((uint32_t *)zrow)[ctid] = 0u;
     const int c = warp - 1;
     const int slot_row = c / a.wk, piece = c % a.wk;
     const int kbase = piece * 32 * LW + 16 * lane;
@@ -396,8 +385,20 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
     }
     grid_dependency_wait();   // X (and Y, written below) belong to the stream order after the preceding kernel
     const uint8_t *tab_lane = tab + 4 * lane;
-    const uint8_t *zero_lane = zrow + 4 * lane;
     asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // bitmap words and zeroed row sums are in place
+    // the CTA's run of verbatim blocks: ranks [v_begin, v_end) of the verbatim stream, the first v_staged of them
+    // staged in shared memory by the producer
+    uint64_t v_begin = 0;
+    uint32_t v_staged = 0;
+    bool v_ready = false;
+    if (FMT == FMT_PAL && nrows) {
+        const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
+        v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
+        const uint64_t lw = (lb >> 5) - wb0;
+        const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
+                                                    : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
+        v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
+    }
     uint32_t xr[NB][LW / 2];  // bf16x2 activations of the lane's weights
 #pragma unroll
     for (int j = 0; j < NB; j++)
@@ -482,11 +483,26 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
         float acc0[NB], acc1[NB];
 #pragma unroll
         for (int j = 0; j < NB; j++) acc0[j] = acc1[j] = 0.f;
+        // The 16 exponents of the verbatim group of the lane whose block is bl (relative to the CTA's first
+        // bitmap word) at K-slice position kk: from the staged run, or from global memory beyond it.
+        auto verbatim_exps = [&](uint32_t bl, int kk) -> uint4 {
+            const uint32_t wd = bl >> 5;
+            const uint64_t rank = (uint64_t)pf[wd] + __popc(bm[wd] & ((1u << (bl & 31)) - 1u));
+            const uint64_t vl = rank - v_begin;
+            const int q = (kk >> 4) & 3;  // the group's quarter of its 64-weight block
+            if (vl < v_staged) {
+                if (!v_ready) {  // the first verbatim group this lane meets: the staged run must have landed
+                    if (!mbar_wait(vfull, 0)) ok = false;
+                    v_ready = true;
+                }
+                return *(const uint4 *)(vx + vl * 64 + 16 * q);
+            }
+            return __ldg((const uint4 *)(a.w.verb_exp + rank * 64 + 16 * q));
+        };
         // The lane's groups of this stage.  BD: some group of the warp lies past the CTA's rows or the K-slice
-        // (those are skipped).  VB: some lane of the warp has a verbatim group; a verbatim group (its codes are
-        // all zero) reads a zero table row under a zero sign+mantissa mask and multiplies zero activations, so it
-        // adds exactly +0 * +0 even where X holds an infinity or a NaN (the pass after the main loop adds its
-        // true product).  Without BD the groups are straight-line code.
+        // (those are skipped).  VB: some lane of the warp has a verbatim group; that lane rebuilds the group from
+        // the block's own exponents instead of the palette (its codes are all zero).  Without BD the groups are
+        // straight-line code.
         auto run_groups = [&](auto BD, auto VB) {
             constexpr bool bd = decltype(BD)::value, vb = decltype(VB)::value;
 #pragma unroll
@@ -494,18 +510,19 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 if (bd && (!live || kbase + 512 * g >= klen)) continue;  // past the CTA's rows or the K-slice
                 if (!kEarly) load_group(g, d0[g], d1[g]);
                 uint32_t pw[8];  // 8 bf16x2 pairs of weights
-                bool vg = false;
                 if (FMT == FMT_PAL) {
-                    vg = vb && ((vwin >> (8 * g)) & 1u);
-                    const uint8_t *tl = vg ? zero_lane : tab_lane;
-                    const uint32_t msk = vg ? 0u : 0x807F807Fu;
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const uint32_t S = word_of(d0[g], q);
                         const uint32_t Cw = q < 2 ? d1[g].x : d1[g].y;
                         const int jb = 2 * (q & 1);
-                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & msk) | pair_exp(tl, Cw, jb);
-                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & msk) | pair_exp(tl, Cw, jb + 1);
+                        pw[2 * q] = (__byte_perm(S, 0u, 0x1100u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb);
+                        pw[2 * q + 1] = (__byte_perm(S, 0u, 0x3322u) & 0x807F807Fu) | pair_exp(tab_lane, Cw, jb + 1);
+                    }
+                    if (vb && ((vwin >> (8 * g)) & 1u)) {
+                        const uint4 E = verbatim_exps(bl0 + 8 * g, kbase + 512 * g);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) pairs_from_exps(word_of(d0[g], q), word_of(E, q), pw[2 * q], pw[2 * q + 1]);
                     }
                 } else if (FMT == FMT_EXP) {
 #pragma unroll
@@ -515,13 +532,12 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
 #pragma unroll
                     for (int q = 0; q < 4; q++) { pw[q] = word_of(d0[g], q); pw[4 + q] = word_of(d1[g], q); }
                 }
-                const uint32_t xm = vg ? 0u : 0xFFFFFFFFu;  // (all ones unless the body handles verbatim groups)
 #pragma unroll
                 for (int j = 0; j < NB; j++)
 #pragma unroll
                     for (int t = 0; t < 8; t += 2) {
-                        acc0[j] = fma2_bf16(pw[t], vb ? xr[j][8 * g + t] & xm : xr[j][8 * g + t], acc0[j]);
-                        acc1[j] = fma2_bf16(pw[t + 1], vb ? xr[j][8 * g + t + 1] & xm : xr[j][8 * g + t + 1], acc1[j]);
+                        acc0[j] = fma2_bf16(pw[t], xr[j][8 * g + t], acc0[j]);
+                        acc1[j] = fma2_bf16(pw[t + 1], xr[j][8 * g + t + 1], acc1[j]);
                     }
             }
         };
@@ -554,94 +570,6 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const __grid_constant_
                 if ((lane & 7) == 0 && si >= (i & ~3) && rw < r1) atomicAdd(&part[(rw - r0) * NB + j], v);
 #pragma unroll
                 for (int t = 0; t < 4; t++) vs[t][j] = 0.f;
-            }
-        }
-    }
-    // Verbatim blocks.  The main loop counted every verbatim block as exactly zero, so no warp ran a slower body
-    // for them and held up the ring.  Their true products are added now.  Once every consumer is done with the
-    // ring, the warps of the first row slot write X (the CTA's K-slice, from their registers) into it; then one
-    // thread per verbatim block reads the block's record (exponents, sign+mantissa bytes, block index: staged in
-    // shared memory, or from global memory beyond the staged ones) and X from shared memory.
-    const bool x_in_ring = (size_t)a.stages * a.stage_bytes >= (size_t)NB * klen * 2;
-    if (FMT == FMT_PAL) {
-        asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // the ring is free
-        if (x_in_ring && slot_row == 0) {
-#pragma unroll
-            for (int j = 0; j < NB; j++)
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    const int kk = kbase + 512 * g;
-                    if (kk >= klen) continue;
-                    uint4 *dst = (uint4 *)(ring + ((size_t)j * klen + kk) * 2);
-                    dst[0] = make_uint4(xr[j][8 * g], xr[j][8 * g + 1], xr[j][8 * g + 2], xr[j][8 * g + 3]);
-                    dst[1] = make_uint4(xr[j][8 * g + 4], xr[j][8 * g + 5], xr[j][8 * g + 6], xr[j][8 * g + 7]);
-                }
-        }
-        asm volatile("bar.sync 1, %0;" ::"r"(CT) : "memory");  // X is in the ring
-        if (nrows && __all_sync(0xFFFFFFFFu, ok)) {
-            const uint64_t fb = (uint64_t)r0 * K / 64, lb = (uint64_t)r1 * K / 64;
-            const uint64_t v_begin = pf[0] + __popc(bm[0] & ((1u << (fb & 31)) - 1u));
-            const uint64_t lw = (lb >> 5) - wb0;
-            const uint64_t v_end = lw < (uint64_t)n_bw ? pf[lw] + __popc(bm[lw] & ((1u << (lb & 31)) - 1u))
-                                                        : pf[n_bw - 1] + __popc(bm[n_bw - 1]);
-            const uint32_t v_staged = (uint32_t)min(v_end - v_begin, (uint64_t)a.vcap);
-            // four threads per block (16 weights each, lanes 4m .. 4m + 3 of a warp); whole warps step together so
-            // the quarter sums can meet by shuffles
-            const uint32_t kpr = (uint32_t)(K / 64);
-            const uint64_t items = 4 * (v_end - v_begin), span = (items + 31) / 32 * 32;
-            bool wok = true;  // warp-uniform: the staged records have landed
-            if ((uint64_t)(ctid - lane) < items && v_staged) wok = mbar_wait(vfull, 0);
-            wok = __all_sync(0xFFFFFFFFu, wok);
-            if (!wok) ok = false;
-            for (uint64_t it = ctid; it < span && wok; it += CT) {
-                const bool has = it < items;
-                const uint64_t v = v_begin + (has ? it >> 2 : 0);
-                const int qd = (int)(it & 3);
-                const uint64_t vl = v - v_begin;
-                const uint8_t *rec = vl < v_staged ? vx + vl * kVerbRec : nullptr;
-                uint32_t blk = 0;
-                if (has) blk = rec ? *(const uint32_t *)(rec + 128) : __ldg((const uint32_t *)(a.w.verb_rec + v * kVerbRec + 128));
-                const uint32_t row = blk / kpr;
-                const int64_t kb = (int64_t)(blk - row * kpr) * 64;
-                const bool live = has && kb >= k0 && kb < k0 + klen;  // else another K-slice's block
-                float s0[NB], s1[NB];
-#pragma unroll
-                for (int j = 0; j < NB; j++) s0[j] = s1[j] = 0.f;
-                if (live) {
-                    const uint4 ev = rec ? *(const uint4 *)(rec + 16 * qd) : __ldg((const uint4 *)(a.w.verb_rec + v * kVerbRec + 16 * qd));
-                    const uint4 sv = rec ? *(const uint4 *)(rec + 64 + 16 * qd)
-                                         : __ldg((const uint4 *)(a.w.verb_rec + v * kVerbRec + 64 + 16 * qd));
-#pragma unroll
-                    for (int j = 0; j < NB; j++) {
-                        if (b0 + j >= a.B) continue;
-                        const int kl = (int)(kb - k0) + 16 * qd;
-                        uint4 xa, xb;
-                        if (x_in_ring) {
-                            const uint4 *xp = (const uint4 *)(ring + ((size_t)j * klen + kl) * 2);
-                            xa = xp[0];
-                            xb = xp[1];
-                        } else {
-                            const uint4 *xp = (const uint4 *)(a.x + (b0 + j) * K + k0 + kl);
-                            xa = __ldg(xp);
-                            xb = __ldg(xp + 1);
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            uint32_t p01, p23;
-                            pairs_from_exps(word_of(sv, q), word_of(ev, q), p01, p23);
-                            const uint4 &xv = q < 2 ? xa : xb;
-                            s0[j] = fma2_bf16(p01, word_of(xv, 2 * (q & 1)), s0[j]);
-                            s1[j] = fma2_bf16(p23, word_of(xv, 2 * (q & 1) + 1), s1[j]);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < NB; j++) {
-                    float t = s0[j] + s1[j];
-                    t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
-                    t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
-                    if (live && qd == 0 && b0 + j < a.B) atomicAdd(&part[(row - r0) * NB + j], t);
-                }
             }
         }
     }
@@ -734,9 +662,9 @@ bool plan_shape(const WOperand &w, int64_t B, int split_k, int max_warps, int pe
     if (fixed + 2 * (size_t)s.stage_bytes > smem_cap) return false;
     s.stages = (int)std::min<size_t>(8, (smem_cap - fixed) / s.stage_bytes);
     s.smem = fixed + (size_t)s.stages * s.stage_bytes;
-    // verbatim records in the shared memory left over (at most 512)
-    s.vcap = w.fmt == FMT_PAL && w.verb_rec ? (int)std::min<size_t>(512, (smem_cap - s.smem) / kVerbRec) : 0;
-    s.smem += (size_t)s.vcap * kVerbRec;
+    // exponents of verbatim blocks in the shared memory left over (at most 1024 blocks)
+    s.vcap = w.fmt == FMT_PAL ? (int)std::min<size_t>(1024, (smem_cap - s.smem) / 64) : 0;
+    s.smem += (size_t)s.vcap * 64;
     return true;
 }
 
@@ -802,8 +730,7 @@ bool plan_variant(const WOperand &w, int64_t B, int split_k, int variant, TmaSha
 bool gemv_tma_supported(const WOperand &w, int64_t B, int variant)
 {
     TmaShape s;
-    // the verbatim pass of 4-bit-code stages reads the verbatim records, built when codes are resident
-    return (w.fmt != FMT_PAL || w.verb_rec) && variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
+    return variant != 1 && B >= 1 && B <= 2 && w.N > 0 && w.K > 0 &&
            plan_variant(w, B, 0, variant, s);
 }
 
@@ -811,7 +738,7 @@ int launch_gemv_tma(const WOperand &w, const uint16_t *x, int64_t B, void *y, in
                     float *acc_ws, int *status, void *stream)
 {
     TmaShape s;
-    if ((w.fmt == FMT_PAL && !w.verb_rec) || !plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
+    if (!plan_variant(w, B, split_k, variant, s)) return cudaErrorInvalidValue;
     const int nb = B <= 1 ? 1 : 2;
     cudaStream_t st = (cudaStream_t)stream;
     TmaArgs a;

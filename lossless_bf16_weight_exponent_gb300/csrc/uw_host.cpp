@@ -449,27 +449,6 @@ uw_status parse_and_validate(const uint8_t *p, size_t size, BlobHeader *out, boo
     return UW_OK;
 }
 
-void build_verbatim_records(const BlobHeader &h, const uint8_t *blob, std::vector<uint8_t> &rec)
-{
-    const uint64_t n = (uint64_t)h.N * (uint64_t)h.K;
-    const uint32_t *bm = (const uint32_t *)(blob + h.off[S_BITMAP]);
-    const uint8_t *ve = blob + h.off[S_VERB];
-    const uint8_t *sm = blob + h.off[S_SM];
-    rec.assign((size_t)h.n_verbatim * kVerbRec, 0);
-    uint64_t vi = 0;
-    for (uint64_t w = 0; w < (h.n_blocks + 31) / 32; w++)
-        for (uint32_t bits = bm[w]; bits; bits &= bits - 1) {
-            const uint64_t b = w * 32 + (uint64_t)__builtin_ctz(bits);
-            if (b >= h.n_blocks || vi >= h.n_verbatim) return;  // a validated blob never gets here
-            uint8_t *r = &rec[vi * kVerbRec];
-            memcpy(r, ve + vi * 64, 64);
-            const uint64_t s0 = b * 64, len = std::min<uint64_t>(64, n - s0);
-            memcpy(r + 64, sm + s0, len);
-            const uint32_t b32 = (uint32_t)b;  // blocks of a matrix fit 32 bits
-            memcpy(r + 128, &b32, 4);
-            vi++;
-        }
-}
 
 void build_tile_verbatim(const BlobHeader &h, const uint8_t *blob, std::vector<uint32_t> &off,
                          std::vector<uint32_t> &mask, std::vector<uint8_t> &data)

@@ -40,10 +40,6 @@ void build_decode_table(const uint8_t *lens, int max_len, std::vector<uint8_t> &
 void build_multi_table(const uint8_t *lens, std::vector<uint32_t> &table);
 // Tile-major verbatim stream of a blob (K % 256 == 0): per unit of 128 rows x 256 weights, a 16-word mask
 // ([K-stage j][row word]) and the count prefix; the verbatim exponents reordered unit by unit, (j, row) order.
-// verbatim records of kVerbRec bytes: for the v-th verbatim block, its 64 exponents, its 64 sign+mantissa bytes and
-// its block index (u32, then 12 zero bytes), so a run of verbatim blocks is one contiguous copy
-constexpr int kVerbRec = 144;
-void build_verbatim_records(const BlobHeader &h, const uint8_t *blob, std::vector<uint8_t> &rec);
 void build_tile_verbatim(const BlobHeader &h, const uint8_t *blob, std::vector<uint32_t> &off,
                          std::vector<uint32_t> &mask, std::vector<uint8_t> &data);
 
@@ -84,7 +80,6 @@ struct WOperand {
     const uint16_t *w;        // FMT_BF16: [N*K]
     const uint32_t *bitmap, *prefix;
     const uint8_t *verb_exp;  // FMT_PAL verbatim handling
-    const uint8_t *verb_rec;  // [n_verbatim * kVerbRec] verbatim records (build_verbatim_records)
     // tile-major verbatim stream (present when K % 256 == 0): for unit u = tile * (K / 256) + kq (128 rows x 256
     // weights), tmv_mask[16u + 4j + w] bit b = row 32w + b's block kq*4 + j is verbatim; its exponents follow
     // those of earlier (j, row) in the unit at tmv_data[64 * (tmv_off[u] + rank)]

@@ -46,7 +46,6 @@ struct uw_matrix {
     uint8_t *codes = nullptr;  // resident 4-bit codes (may be null for Huffman)
     const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
     const uint8_t *tmv_data = nullptr;
-    const uint8_t *verb_rec = nullptr;
     bool has_stream = false;  // the Huffman stream (offsets, bits, tables) is resident
     int device = 0;
     std::mutex mu;
@@ -133,11 +132,6 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int resident, uw_str
     const uint64_t o_tmo = tmv ? take(tmv_off.size() * 4 + 16) : 0;
     const uint64_t o_tmm = tmv ? take(tmv_mask.size() * 4 + 16) : 0;
     const uint64_t o_tmd = tmv ? take(tmv_data.size() + 64) : 0;
-    // verbatim records (exponents + sign+mantissa bytes per verbatim block) for the bulk-copy GEMV's verbatim
-    // pass, which reads 4-bit codes: built when codes are resident
-    std::vector<uint8_t> vrec;
-    if (resident_codes) build_verbatim_records(h, p, vrec);
-    const uint64_t o_vr = resident_codes ? take(vrec.size() + 64) : 0;
 
     uw_matrix *m = new (std::nothrow) uw_matrix();
     if (!m) return fail(UW_ERR_NO_MEMORY, "uw_load: host allocation");
@@ -173,8 +167,6 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int resident, uw_str
                 (!tmv_data.empty() &&
                  (e = cudaMemcpyAsync(d + o_tmd, tmv_data.data(), tmv_data.size(), cudaMemcpyHostToDevice, st)))))
         return fail_free(cuda_fail(e, "uw_load: verbatim stream upload"));
-    if (!vrec.empty() && (e = cudaMemcpyAsync(d + o_vr, vrec.data(), vrec.size(), cudaMemcpyHostToDevice, st)))
-        return fail_free(cuda_fail(e, "uw_load: verbatim record upload"));
     std::vector<uint8_t> table;
     std::vector<uint32_t> mtable;
     if (huff) {
@@ -208,7 +200,6 @@ extern "C" uw_status uw_load(const void *blob, size_t size, int resident, uw_str
     m->tmv_off = tmv ? (const uint32_t *)(d + o_tmo) : nullptr;
     m->tmv_mask = tmv ? (const uint32_t *)(d + o_tmm) : nullptr;
     m->tmv_data = tmv ? d + o_tmd : nullptr;
-    m->verb_rec = resident_codes ? d + o_vr : nullptr;
     m->has_stream = resident_stream;
     if (huff && resident_codes) {
         // the post's load-time transcode of the Huffman stream into the direct-palette form
@@ -333,7 +324,6 @@ static WOperand operand_shape(const uw_matrix *m, int strategy)
     w.tmv_off = m->tmv_off;
     w.tmv_mask = m->tmv_mask;
     w.tmv_data = m->tmv_data;
-    w.verb_rec = m->verb_rec;
     w.codes = m->codes;
     w.status = m->v.status;
     return w;
