@@ -461,54 +461,84 @@ def measure_workload(cfg, mat, batches, resident, stream, hbm, tf_peak, blob=Non
     return out
 
 
-def measure_stack(layers, batches, stream, hbm, tf_peak, resident="palette"):
+def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)):
     """The 8B MLP stack: gate, up, down per layer (per-layer seeds), one graph per pass over all 3 x layers
-    matmuls; the gate/up shape and the down shape are autotuned once each and the tables shared by shape."""
+    matmuls.  All layers easy (palette form resident, AUTO: direct palette); then hard layers (the Huffman stream
+    alone, transcoded on a side stream into double-buffered slots by uw_sequence_run) every k-th layer; then every
+    matrix as the Huffman stream alone under AUTO (the Huffman-direct GEMV up to B = 8).  The gate/up shape and the
+    down shape are autotuned once each per form and the tables shared by shape."""
     import torch
 
     import lossless_bf16_weight_exponent_gb300 as uw
     import synth
     recipes = synth.stack_8b(layers)
     blobs = encode_many(recipes)
-    mats = [uw.Matrix(b, resident=resident) for b in blobs]
+    pal = [uw.Matrix(b, resident="palette") for b in blobs]
+    huf = [uw.Matrix(b, resident="huffman") for b in blobs]
     del blobs
-    infos = [m.info for m in mats]
-    tables = {}
-    for first in (0, 2):
-        need = mats[first].autotune_workspace_size(batches)
-        tws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
-        mats[first].autotune(batches, tws, need)
-        del tws
-        tables[first] = mats[first].tune_save()
-    for i, m in enumerate(mats):
-        m.tune_load(tables[0 if i % 3 != 2 else 2])
+    for mats in (pal, huf):
+        for first in (0, 2):
+            need = mats[first].autotune_workspace_size(batches)
+            tws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
+            mats[first].autotune(batches, tws, need)
+            del tws
+            table = mats[first].tune_save()
+            for i in range(first, len(mats), 3) if first == 2 else [i for i in range(len(mats)) if i % 3 != 2]:
+                mats[i].tune_load(table)
+    bf16_bytes = sum(2 * m.info["N"] * m.info["K"] for m in pal)
+    side = torch.cuda.Stream()
     out = []
     for B in batches:
-        ws_bytes = max(m.workspace_size(B) for m in mats[:3])
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
         x_in = torch.from_numpy(recipes[0].activations(B).view(np.int16)).cuda()            # [B, 4096]
         x_mid = torch.from_numpy(recipes[2].activations(B).view(np.int16)).cuda()           # [B, 14336]
         y_mid = torch.empty((B, 14336), dtype=torch.float32, device="cuda")
         y_out = torch.empty((B, 4096), dtype=torch.float32, device="cuda")
 
-        def call(i, s):
-            if i % 3 == 2:
-                mats[i].matmul(x_mid, B, y_out, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
-            else:
-                mats[i].matmul(x_in, B, y_mid, uw.OUT_F32, uw.STRAT_AUTO, ws, ws_bytes, s)
-        us = time_graph(call, len(mats), 5, stream)
-        strat = 4 if infos[0]["has_palette_form"] else 5
-        comp = sum(algorithmic_bytes(inf, strat, B) for inf in infos)
-        eff = sum(2 * inf["N"] * inf["K"] + 2 * B * inf["K"] + 4 * B * inf["N"] for inf in infos)
-        flops = sum(2.0 * B * inf["N"] * inf["K"] for inf in infos)
-        out.append(point_line("stack_8b", f"{layers} layers x (gate, up W[14336,4096]; down W[4096,14336])", B, us,
-                              comp, eff, flops,
-                              {"gate_up": mats[0].plan_for(B).as_tuple(), "down": mats[2].plan_for(B).as_tuple()},
-                              hbm, tf_peak,
-                              {"matmuls": len(mats), "us_per_matmul": round(us / len(mats), 2), "resident": resident,
-                               "resident_ratio": round(sum(i["device_bytes"] for i in infos) /
-                                                       sum(2 * i["N"] * i["K"] for i in infos), 4)}))
-    del mats
+        def steps_of(mats):
+            return [(m, x_mid if i % 3 == 2 else x_in, y_out if i % 3 == 2 else y_mid, uw.OUT_F32)
+                    for i, m in enumerate(mats)]
+        flops = sum(2.0 * B * m.info["N"] * m.info["K"] for m in pal)
+        eff = sum(2 * m.info["N"] * m.info["K"] + 2 * B * m.info["K"] + 4 * B * m.info["N"] for m in pal)
+        patterns = [("all easy", 0)] + [(f"hard every {k}", k) for k in hard_every]
+        base_us = None
+        for name, k in patterns:
+            mats = [huf[i] if k and (i // 3) % k == k - 1 else pal[i] for i in range(len(pal))]
+            steps = steps_of(mats)
+            need = uw.sequence_workspace_size(steps, B)
+            wsb = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+            wsp = (wsb.data_ptr() + 255) // 256 * 256
+            hard = sum(1 for m in mats if not m.info["has_palette_form"])
+            d = uw.sequence_tune(steps, B, wsp, need, stream, side) if hard else 0  # the decode-vs-matmul SM split
+            us = time_graph(lambda i, s: uw.sequence_run(steps, B, wsp, need, s, side, d), 1, 5, stream)
+            resident = sum(m.info["device_bytes"] for m in mats) + (need if hard else 0)
+            base_us = base_us or us
+            comp = sum(algorithmic_bytes(m.info, 4 if m.info["has_palette_form"] else 3, B) for m in mats)
+            out.append(point_line("stack_8b", f"{layers} layers x (gate, up W[14336,4096]; down W[4096,14336])", B,
+                                  us, comp, eff, flops,
+                                  {"gate_up": pal[0].plan_for(B).as_tuple(), "down": pal[2].plan_for(B).as_tuple()},
+                                  hbm, tf_peak,
+                                  {"schedule": name, "matmuls": len(mats), "hard_matmuls": hard, "decode_sms": d,
+                                   "us_per_matmul": round(us / len(mats), 2), "time_vs_all_easy": round(us / base_us, 3),
+                                   "resident_ratio": round(resident / bf16_bytes, 4),
+                                   "api": "uw_sequence_run (hard steps transcoded on a side stream)"}))
+            del wsb
+        # every matrix as the Huffman stream alone, AUTO plan per call
+        if B <= 8:
+            ws_bytes = max(m.workspace_size(B) for m in huf[:3])
+            ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+
+            def call(i, s):
+                huf[i].matmul(x_mid if i % 3 == 2 else x_in, B, y_out if i % 3 == 2 else y_mid, uw.OUT_F32,
+                              uw.STRAT_AUTO, ws, ws_bytes, s)
+            us = time_graph(call, len(huf), 5, stream)
+            comp = sum(algorithmic_bytes(m.info, 5, B) for m in huf)
+            out.append(point_line("stack_8b", f"{layers} layers x (gate, up W[14336,4096]; down W[4096,14336])", B,
+                                  us, comp, eff, flops, {"all": huf[0].plan_for(B).as_tuple()}, hbm, tf_peak,
+                                  {"schedule": "all Huffman stream alone (AUTO)", "matmuls": len(huf),
+                                   "us_per_matmul": round(us / len(huf), 2), "time_vs_all_easy": round(us / base_us, 3),
+                                   "resident_ratio": round(sum(m.info["device_bytes"] for m in huf) / bf16_bytes, 4)}))
+            del ws
+    del pal, huf
     torch.cuda.empty_cache()
     return out
 
@@ -805,7 +835,7 @@ def run_sweep(args):
     for cfg, mat, bs, resident in single:
         for d in measure_workload(cfg, mat, bs, resident, stream, hbm, tf_peak):
             print(json.dumps(d), flush=True)
-    for d in measure_stack(args.stack_layers, [1, 8, 32, 128], stream, hbm, tf_peak):
+    for d in measure_stack(args.stack_layers, [1, 8, 32, 128], stream, hbm, tf_peak, hard_every=(8, 4, 2)):
         print(json.dumps(d), flush=True)
 
 

@@ -320,6 +320,48 @@ uw_status uw_autotune_workspace_size(const uw_matrix *m, const int64_t *batches,
 uw_status uw_tune_save(const uw_matrix *m, char *buf, size_t cap, size_t *len);
 uw_status uw_tune_load(uw_matrix *m, const char *text);
 
+/* One matmul of a sequence: Y[B,N] = X[B,K] . W^T for the loaded matrix m; x and y are device pointers as in
+ * uw_matmul, out_dtype a uw_out_dtype; reserved must be 0. */
+typedef struct {
+    const uw_matrix *m;
+    const uint16_t *x;
+    void *y;
+    int32_t out_dtype;
+    int32_t reserved;
+} uw_step;
+
+/*
+ * uw_sequence_run - run n matmuls in order at batch B (the post's section on scheduling hard and easy layers).
+ *   A step is "hard" when its matrix holds only its Huffman stream (UW_RESIDENT_HUFFMAN): its 4-bit palette codes
+ *   are transcoded on `side_stream` into one of two slots of the workspace (double buffering), as soon as the
+ *   slot's previous matmul is done, so the transcode of the next hard step runs while the main stream works on
+ *   the steps before it.  Its matmul on `stream` waits for that transcode and reads the codes (the direct-palette
+ *   kernels).  Steps whose matrix holds its palette form run their AUTO plan.  Asynchronous: everything is enqueued
+ *   at once and ordered by events; `stream` ends joined with `side_stream`, so the call can be captured into one
+ *   CUDA graph from `stream`.  `side_stream` must differ from `stream` when a step is hard.  The workspace
+ *   (uw_sequence_workspace_size bytes, 256-byte aligned) belongs to the sequence until `stream` has passed it.
+ *   The first call in a thread on a device creates the events the calls use; make it before any stream capture.
+ *   The steps' x and y must not overlap a later step's inputs unless the caller wants that chaining: steps run in
+ *   order on `stream`.
+ *   Errors: UW_ERR_INVALID_ARG, UW_ERR_WORKSPACE, UW_ERR_CUDA, or a step's uw_matmul error.
+ */
+/*   decode_sms: the post's decode-vs-matmul SM split.  0: every launch sizes its grid for all SMs.  d > 0: the
+ *   main stream's persistent matmul grids are sized for the device's SMs minus d, and each transcode is a
+ *   persistent grid of d SMs' worth of CTAs, so the two run side by side.  Must lie in [0, SMs).
+ */
+uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int64_t B, size_t *bytes);
+uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
+                          uw_stream side_stream, int decode_sms);
+
+/*
+ * uw_sequence_tune - time uw_sequence_run over these steps (same arguments) for a range of decode SM splits
+ *   (0, 8, 16, ..., 96; CUDA events on `stream`, median of three runs after two) and return the fastest split in
+ *   *decode_sms (the post's tuning of the decoder's share of the SMs).  Synchronous; runs the sequence 5 times per
+ *   split, writing the steps' outputs.
+ */
+uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
+                           uw_stream side_stream, int *decode_sms);
+
 /* uw_check - synchronise `stream` and report (then clear) the matrix's device status word. */
 uw_status uw_check(const uw_matrix *m, uw_stream stream);
 

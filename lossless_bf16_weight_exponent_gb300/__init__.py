@@ -53,6 +53,11 @@ class Plan(ctypes.Structure):
         return f"Plan(strategy={self.strategy}, kernel={self.kernel}, split_k={self.split_k}, variant={self.variant})"
 
 
+class Step(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("out_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
 class Info(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("codec", ctypes.c_uint32), ("n_pal", ctypes.c_uint32),
                 ("palette", ctypes.c_uint8 * 16), ("code_len", ctypes.c_uint8 * 16),
@@ -92,6 +97,9 @@ _SIGS = {
     "uw_tune_load": [_VP, ctypes.c_char_p],
     "uw_check": [_VP, _VP],
     "uw_matmul_noalloc": [_VP, _VP, _I64, _VP, _INT, _VP],
+    "uw_sequence_workspace_size": [ctypes.POINTER(Step), _INT, _I64, ctypes.POINTER(_SZ)],
+    "uw_sequence_run": [ctypes.POINTER(Step), _INT, _I64, _VP, _SZ, _VP, _VP, _INT],
+    "uw_sequence_tune": [ctypes.POINTER(Step), _INT, _I64, _VP, _SZ, _VP, _VP, ctypes.POINTER(_INT)],
     "uw_status_string": [_INT],
     "uw_last_error": [],
     "uw_version": [],
@@ -263,3 +271,34 @@ class Matrix:
 
     def check(self, stream=None):
         _check(lib().uw_check(self._h, _stream(stream)), "uw_check")
+
+
+def _steps(steps):
+    arr = (Step * max(1, len(steps)))()
+    for i, st in enumerate(steps):
+        m, x, y = st[0], st[1], st[2]
+        od = st[3] if len(st) > 3 else OUT_F32
+        arr[i] = Step(m.handle.value if isinstance(m, Matrix) else m, _ptr(x), _ptr(y), od, 0)
+    return arr
+
+
+def sequence_workspace_size(steps, B: int) -> int:
+    """Workspace bytes of uw_sequence_run; steps: (Matrix, x, y[, out_dtype]) tuples."""
+    n = ctypes.c_size_t(0)
+    _check(lib().uw_sequence_workspace_size(_steps(steps), len(steps), B, ctypes.byref(n)), "uw_sequence_workspace_size")
+    return n.value
+
+
+def sequence_run(steps, B: int, workspace, ws_bytes: int, stream=None, side_stream=None, decode_sms: int = 0):
+    """uw_sequence_run: the steps in order on `stream`, hard steps' transcodes on `side_stream` (on `decode_sms`
+    SMs beside the matmuls when it is > 0)."""
+    _check(lib().uw_sequence_run(_steps(steps), len(steps), B, _ptr(workspace), ws_bytes, _stream(stream),
+                                 _stream(side_stream), decode_sms), "uw_sequence_run")
+
+
+def sequence_tune(steps, B: int, workspace, ws_bytes: int, stream=None, side_stream=None) -> int:
+    """uw_sequence_tune: the fastest decode SM split for these steps."""
+    d = ctypes.c_int(0)
+    _check(lib().uw_sequence_tune(_steps(steps), len(steps), B, _ptr(workspace), ws_bytes, _stream(stream),
+                                  _stream(side_stream), ctypes.byref(d)), "uw_sequence_tune")
+    return d.value

@@ -149,12 +149,24 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
     }
     for (int i = threadIdx.x; i < 256; i += blockDim.x)
         pal2[i] = (uint16_t)(v.palette[i & 15] | (v.palette[i >> 4] << 8));
-    const uint64_t c_first = (uint64_t)blockIdx.x * kDecThreads;
-    const uint64_t c_last = min((uint64_t)v.n_chunks, c_first + kDecThreads);
     __syncthreads();
+    // a persistent grid (fewer CTAs than groups of kDecThreads chunks, when it is given a share of the SMs) walks
+    // the groups with a stride
+    for (uint64_t c_first = (uint64_t)blockIdx.x * kDecThreads; c_first < v.n_chunks;
+         c_first += (uint64_t)gridDim.x * kDecThreads) {
+    const uint64_t c_last = min((uint64_t)v.n_chunks, c_first + kDecThreads);
+    if (threadIdx.x == 0) {
+        // the CTA's chunks are one contiguous run of the stream: one bulk prefetch into L2, so each thread's
+        // first read of a 32-byte sector finds it there instead of in DRAM
+        const uint32_t b0 = (__ldg(v.chunk_off + c_first) >> 3) & ~15u;
+        const uint32_t b1 = (uint32_t)((((uint64_t)__ldg(v.chunk_off + c_last) + 127u) >> 7) << 4);
+        if (b1 > b0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const uint8_t *)v.bits + b0), "r"(b1 - b0)
+                         : "memory");
+    }
     const uint8_t *dt = (const uint8_t *)mt;
     const uint64_t c = c_first + threadIdx.x;
-    if (c >= c_last) return;
+    if (c >= c_last) continue;
     // next 32-bit word of the stream (absolute word number); a corrupt stream that runs past the stream's end and
     // its 512-byte guard reads zeros there, and the chunk's length check reports it
     const uint32_t w_lim = ((v.chunk_off[v.n_chunks] + 31) >> 5) + 120;
@@ -284,13 +296,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
         if (used > budget) bad = true;  // overran the chunk: stop before reading further
     }
     if (bad || used != budget) atomicExch(v.status, (int)DEV_CORRUPT);
+    }
 }
 
-int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream)
+int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream, int max_ctas)
 {
     if (!v.n_chunks) return cudaSuccess;
     const int threads = kDecThreads;
-    const int blocks = (int)((v.n_chunks + threads - 1) / threads);
+    int blocks = (int)((v.n_chunks + threads - 1) / threads);
+    if (max_ctas > 0) blocks = std::min(blocks, max_ctas);
     const size_t tab_bytes = v.mtab ? 16384 : std::max<size_t>(16384, (size_t)1 << v.max_len);
     const size_t smem = tab_bytes;  // decode table
     cudaStream_t st = (cudaStream_t)stream;

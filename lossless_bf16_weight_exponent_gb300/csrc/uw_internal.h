@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -93,7 +94,10 @@ struct WOperand {
 
 // kernel launchers (k_decode.cu, k_gemv.cu, k_tc.cu); return cudaError_t as int
 int launch_decode_palette(const DevView &v, int out_kind, void *out, void *stream);
-int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream);
+// max_ctas > 0: at most that many CTAs (a persistent grid over the chunk groups, for a share of the SMs)
+int launch_decode_huffman(const DevView &v, int out_kind, void *out, void *stream, int max_ctas = 0);
+// CTAs of the Huffman decode that one SM holds at once (its shared-memory table limits them)
+constexpr int kDecodeCtasPerSm = 12;
 int launch_gemv(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k,
                 int variant, float *acc_ws, void *stream);
 // persistent bulk-copy GEMV (B <= 2); variant 0: 8 consumer warps, 2 CTAs/SM; 2: 16 warps, 1 CTA/SM with all
@@ -130,8 +134,48 @@ int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_
 bool tc_supported(const WOperand &w, int64_t B, int variant);
 int gemv_default_split(const WOperand &w, int64_t B);
 int tc_default_split(const WOperand &w, int64_t B, int variant);
+// SMs the calling thread's launches size their grids for: the device's, or fewer while an SmBudget is alive
 int num_sms();
+int device_sms();
+// While alive, the calling thread's matmul launches size their persistent grids for n SMs (the decode-vs-matmul
+// split: the remaining SMs are left to a concurrent decode).  Budgets nest; n <= 0 means no limit.
+struct SmBudget {
+    int prev;
+    explicit SmBudget(int n);
+    ~SmBudget();
+    SmBudget(const SmBudget &) = delete;
+    SmBudget &operator=(const SmBudget &) = delete;
+};
 // cuTensorMapEncodeTiled from the driver (nullptr when the driver lacks it)
 void *tensor_map_encoder();
 
+// One autotuned plan per batch bucket (a power of two).
+struct TuneEntry {
+    int64_t bucket;
+    uw_plan plan;
+    float us;
+};
+
+// The matmul of the palette-transcode pipeline with the 4-bit codes already transcoded into `codes` (by an earlier
+// launch, on any stream, ordered before this one by the caller): no preprocess launch, and `ws` holds only the
+// accumulator the kernel may need (matmul_with_codes_workspace bytes).  The matrix must hold its Huffman stream.
+size_t matmul_with_codes_workspace(const uw_matrix *m, int64_t B);
+uw_status matmul_with_codes(const uw_matrix *m, const uint8_t *codes, const uint16_t *x, int64_t B, void *y,
+                            uw_out_dtype od, void *ws, size_t ws_bytes, void *stream);
+
 }  // namespace uw
+
+// A compressed matrix resident on one device.
+struct uw_matrix {
+    uw::BlobHeader h;
+    uw::DevView v;
+    void *dev = nullptr;
+    size_t dev_bytes = 0;
+    uint8_t *codes = nullptr;  // resident 4-bit codes (may be null for Huffman)
+    const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
+    const uint8_t *tmv_data = nullptr;
+    bool has_stream = false;  // the Huffman stream (offsets, bits, tables) is resident
+    int device = 0;
+    std::mutex mu;
+    std::vector<uw::TuneEntry> tune;
+};

@@ -21,12 +21,6 @@ using namespace uw;
 
 namespace {
 
-struct TuneEntry {
-    int64_t bucket;
-    uw_plan plan;
-    float us;
-};
-
 uint64_t round_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 
 int64_t bucket_of(int64_t B)
@@ -38,23 +32,9 @@ int64_t bucket_of(int64_t B)
 
 }  // namespace
 
-struct uw_matrix {
-    BlobHeader h;
-    DevView v;
-    void *dev = nullptr;
-    size_t dev_bytes = 0;
-    uint8_t *codes = nullptr;  // resident 4-bit codes (may be null for Huffman)
-    const uint32_t *tmv_off = nullptr, *tmv_mask = nullptr;  // tile-major verbatim stream (K % 256 == 0)
-    const uint8_t *tmv_data = nullptr;
-    bool has_stream = false;  // the Huffman stream (offsets, bits, tables) is resident
-    int device = 0;
-    std::mutex mu;
-    std::vector<TuneEntry> tune;
-};
-
 namespace uw {
 
-int num_sms()
+int device_sms()
 {
     static int cached[64] = {0};
     int dev = 0;
@@ -67,6 +47,17 @@ int num_sms()
     }
     return cached[dev];
 }
+
+static thread_local int t_sm_budget = 0;
+
+int num_sms()
+{
+    const int n = device_sms();
+    return t_sm_budget > 0 ? std::min(t_sm_budget, n) : n;
+}
+
+SmBudget::SmBudget(int n) : prev(t_sm_budget) { t_sm_budget = n; }
+SmBudget::~SmBudget() { t_sm_budget = prev; }
 
 }  // namespace uw
 
@@ -506,6 +497,39 @@ extern "C" uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x, int64
     if (e) return cuda_fail((cudaError_t)e, "uw_matmul: matmul launch");
     return UW_OK;
 }
+
+namespace uw {
+
+size_t matmul_with_codes_workspace(const uw_matrix *m, int64_t B)
+{
+    const uw_plan p = default_plan_for_strategy(m, std::max<int64_t>(B, 1), UW_STRAT_PALETTE_TRANSCODE);
+    int kernel;
+    if (check_plan(m, std::max<int64_t>(B, 1), p, &kernel) != UW_OK) return 0;
+    return split_bytes(m, std::max<int64_t>(B, 1), p, kernel);
+}
+
+uw_status matmul_with_codes(const uw_matrix *m, const uint8_t *codes, const uint16_t *x, int64_t B, void *y,
+                            uw_out_dtype od, void *ws, size_t ws_bytes, void *stream)
+{
+    if (B == 0 || m->h.N == 0) return UW_OK;
+    const uw_plan p = default_plan_for_strategy(m, B, UW_STRAT_PALETTE_TRANSCODE);
+    int kernel;
+    uw_status s = check_plan(m, B, p, &kernel);
+    if (s != UW_OK) return s;
+    const uint64_t need = split_bytes(m, B, p, kernel);
+    if (ws_bytes < need || (need && !ws))
+        return fail(UW_ERR_WORKSPACE, "matmul workspace %zu bytes, need %llu", ws_bytes, (unsigned long long)need);
+    WOperand w = operand_shape(m, UW_STRAT_PALETTE_TRANSCODE);
+    w.codes = codes;
+    w.w_from_prev = 0;  // written by a launch the caller ordered before this one (another stream's kernel)
+    float *acc = (float *)ws;
+    const int e = kernel == UW_KERNEL_TC ? launch_tc(w, x, B, y, od == UW_OUT_BF16, p.split_k, p.variant, acc, stream)
+                                         : launch_gemv(w, x, B, y, od == UW_OUT_BF16, p.split_k, p.variant, acc, stream);
+    if (e) return cuda_fail((cudaError_t)e, "matmul launch");
+    return UW_OK;
+}
+
+}  // namespace uw
 
 extern "C" uw_status uw_matmul(const uw_matrix *m, const uint16_t *x, int64_t B, void *y, uw_out_dtype od,
                                uw_strategy strategy, void *ws, size_t ws_bytes, uw_stream stream)

@@ -1,0 +1,223 @@
+// uw_sequence.cu - a sequence of matmuls with the Huffman decode of "hard" matrices on a side stream.
+//
+// Cloudflare blog "Unweight", section on scheduling the pipelines: MLP layers alternate between "hard" ones, held
+// Huffman-coded and needing a preprocess, and "easy" ones, held in the pre-transcoded palette form.  While the
+// main stream runs attention and the easy layers, the next hard layer's weights are decoded on other CUDA streams
+// into preprocess slots that are double-buffered; the down projection, consumed last in a layer, has the longest
+// runway.  Here a step is hard when its matrix holds only its Huffman stream: its 4-bit codes are transcoded on
+// the side stream into one of two slots of the workspace as soon as the slot is free (the matmul that read it two
+// hard steps earlier is done), and the main stream's matmul waits only for that transcode.  Easy steps run their
+// AUTO plan.  Everything is enqueued at once and ordered by events; the main stream ends joined with the side
+// stream, so the whole sequence can be captured in one CUDA graph from the main stream.
+//
+// The section on the decode kernels adds that the decoder and the matmul cannot share an SM on H100 (the matmul's
+// shared memory leaves no room for the decoder's table), so the SMs are split between them and the split is tuned.
+// Here `decode_sms` d > 0 sizes the main stream's persistent matmul grids for the device's SMs minus d and gives the
+// transcode a persistent grid of d SMs' worth of CTAs, so the two run side by side; uw_sequence_tune times a
+// range of d and returns the fastest.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <utility>
+#include <vector>
+
+#include "uw_internal.h"
+
+using namespace uw;
+
+namespace {
+
+uint64_t round_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+bool is_hard(const uw_matrix *m) { return m->codes == nullptr && m->has_stream; }
+
+uint64_t slot_bytes_of(const uw_matrix *m) { return round_up((uint64_t)m->h.N * (uint64_t)m->h.K / 2 + 64, 256); }
+
+struct Layout {
+    uint64_t slot;  // bytes of one preprocess slot (the largest hard matrix's codes)
+    uint64_t mm;    // bytes of the matmul workspace (the largest any step needs)
+    int hard;       // hard steps
+};
+
+uw_status layout_of(const uw_step *steps, int n, int64_t B, Layout *L)
+{
+    L->slot = L->mm = 0;
+    L->hard = 0;
+    for (int i = 0; i < n; i++) {
+        const uw_matrix *m = steps[i].m;
+        if (!m) return fail(UW_ERR_INVALID_ARG, "uw_sequence: step %d has no matrix", i);
+        if (is_hard(m)) {
+            L->hard++;
+            L->slot = std::max(L->slot, slot_bytes_of(m));
+            L->mm = std::max<uint64_t>(L->mm, round_up(matmul_with_codes_workspace(m, B), 256));
+        } else {
+            size_t b = 0;
+            uw_status s = uw_workspace_size(m, B, UW_STRAT_AUTO, &b);
+            if (s != UW_OK) return s;
+            L->mm = std::max<uint64_t>(L->mm, round_up(b, 256));
+        }
+    }
+    return UW_OK;
+}
+
+// The six events a sequence uses, one set per thread and device, created by the thread's first call on that
+// device and kept (a call captured into a CUDA graph then creates nothing).  Reusing them across calls is safe: a
+// stream wait binds to the event's latest record when the wait is enqueued, and every wait of a call follows its
+// own records.
+using EventSet = std::array<cudaEvent_t, 6>;
+uw_status thread_events(EventSet **out)
+{
+    thread_local std::vector<std::pair<int, EventSet>> sets;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(UW_ERR_CUDA, "uw_sequence_run: cudaGetDevice: %s", cudaGetErrorString(e));
+    for (auto &p : sets)
+        if (p.first == dev) { *out = &p.second; return UW_OK; }
+    EventSet es{};
+    for (auto &ev : es)
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) {
+            for (auto &d : es)
+                if (d) cudaEventDestroy(d);
+            return fail(UW_ERR_CUDA, "uw_sequence_run: event creation: %s", cudaGetErrorString(e));
+        }
+    sets.emplace_back(dev, es);
+    *out = &sets.back().second;
+    return UW_OK;
+}
+
+}  // namespace
+
+extern "C" uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int64_t B, size_t *bytes)
+{
+    clear_error();
+    if (!bytes || n < 0 || (n && !steps) || B < 0) return fail(UW_ERR_INVALID_ARG, "uw_sequence_workspace_size: bad arguments");
+    Layout L;
+    uw_status s = layout_of(steps, n, B, &L);
+    if (s != UW_OK) return s;
+    *bytes = (L.hard ? 2 * L.slot : 0) + L.mm;
+    return UW_OK;
+}
+
+extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, void *ws, size_t ws_bytes, uw_stream stream,
+                                     uw_stream side_stream, int decode_sms)
+{
+    clear_error();
+    if (n < 0 || (n && !steps) || B < 0) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: bad arguments");
+    if (decode_sms < 0 || decode_sms >= device_sms())
+        return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: decode_sms %d outside [0, %d)", decode_sms, device_sms());
+    if (n == 0 || B == 0) return UW_OK;
+    Layout L;
+    uw_status s = layout_of(steps, n, B, &L);
+    if (s != UW_OK) return s;
+    const uint64_t need = (L.hard ? 2 * L.slot : 0) + L.mm;
+    if (ws_bytes < need || (need && !ws)) return fail(UW_ERR_WORKSPACE, "uw_sequence_run: workspace %zu bytes, need %llu", ws_bytes, (unsigned long long)need);
+    if (ws && ((uintptr_t)ws & 255)) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: workspace not 256-byte aligned");
+    if (L.hard && (stream == side_stream))
+        return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: the side stream must differ from the main stream");
+    for (int i = 0; i < n; i++)
+        if (steps[i].out_dtype != UW_OUT_F32 && steps[i].out_dtype != UW_OUT_BF16)
+            return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: step %d has a bad output dtype", i);
+    uint8_t *slot[2] = {(uint8_t *)ws, (uint8_t *)ws + L.slot};
+    uint8_t *mm = (uint8_t *)ws + (L.hard ? 2 * L.slot : 0);
+    cudaStream_t main = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
+
+    if (!L.hard) {
+        for (int i = 0; i < n; i++) {
+            s = uw_matmul(steps[i].m, steps[i].x, B, steps[i].y, (uw_out_dtype)steps[i].out_dtype, UW_STRAT_AUTO, mm, L.mm,
+                          stream);
+            if (s != UW_OK) return s;
+        }
+        return UW_OK;
+    }
+
+    // events: the side stream starts after the work already on the main stream; ready[k] - slot k holds the codes of
+    // the hard step that uses it next; freed[k] - the matmul that read slot k is done; done - the side stream's end
+    EventSet *ev = nullptr;
+    s = thread_events(&ev);
+    if (s != UW_OK) return s;
+    cudaEvent_t start = (*ev)[0], ready[2] = {(*ev)[1], (*ev)[2]}, freed[2] = {(*ev)[3], (*ev)[4]}, done = (*ev)[5];
+    std::vector<int> hard;
+    for (int i = 0; i < n; i++)
+        if (is_hard(steps[i].m)) hard.push_back(i);
+    // the split: the matmuls' grids for the SMs left, the transcode's for d SMs
+    SmBudget budget(decode_sms ? device_sms() - decode_sms : 0);
+    const int decode_ctas = decode_sms * kDecodeCtasPerSm;
+    cudaError_t e = cudaEventRecord(start, main);
+    if (!e) e = cudaStreamWaitEvent(side, start, 0);
+    // the transcode of hard step j into slot j % 2, on the side stream, once the matmul of hard step j - 2 is done
+    auto enqueue_transcode = [&](int j) -> cudaError_t {
+        const int k = j & 1;
+        cudaError_t r = cudaSuccess;
+        if (j >= 2) r = cudaStreamWaitEvent(side, freed[k], 0);
+        if (!r) r = (cudaError_t)launch_decode_huffman(steps[hard[j]].m->v, DEC_CODES, slot[k], side, decode_ctas);
+        if (!r) r = cudaEventRecord(ready[k], side);
+        return r;
+    };
+    for (int j = 0; j < std::min<int>(2, (int)hard.size()) && !e; j++) e = enqueue_transcode(j);
+    int hj = 0;
+    for (int i = 0; i < n && !e && s == UW_OK; i++) {
+        const uw_step &st = steps[i];
+        if (hj < (int)hard.size() && hard[hj] == i) {
+            const int k = hj & 1;
+            e = cudaStreamWaitEvent(main, ready[k], 0);
+            if (!e) s = matmul_with_codes(st.m, slot[k], st.x, B, st.y, (uw_out_dtype)st.out_dtype, mm, L.mm, main);
+            if (!e && s == UW_OK) e = cudaEventRecord(freed[k], main);
+            if (!e && s == UW_OK && hj + 2 < (int)hard.size()) e = enqueue_transcode(hj + 2);
+            hj++;
+        } else {
+            s = uw_matmul(st.m, st.x, B, st.y, (uw_out_dtype)st.out_dtype, UW_STRAT_AUTO, mm, L.mm, stream);
+        }
+    }
+    // join: the main stream ends after the side stream's last transcode
+    if (!e) e = cudaEventRecord(done, side);
+    if (!e) e = cudaStreamWaitEvent(main, done, 0);
+    if (e) return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
+    return s;
+}
+
+extern "C" uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, void *ws, size_t ws_bytes, uw_stream stream,
+                                      uw_stream side_stream, int *decode_sms)
+{
+    clear_error();
+    if (!decode_sms) return fail(UW_ERR_INVALID_ARG, "uw_sequence_tune: decode_sms is NULL");
+    *decode_sms = 0;
+    if (n == 0 || B == 0) return UW_OK;
+    cudaStream_t main = (cudaStream_t)stream;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return fail(UW_ERR_CUDA, "uw_sequence_tune: event creation failed");
+    }
+    const int sms = device_sms();
+    float best = 3.0e38f;
+    uw_status result = UW_OK;
+    for (int d : {0, 8, 16, 24, 32, 40, 48, 64, 80, 96}) {
+        if (d >= sms) continue;
+        float t[3];
+        bool ok = true;
+        for (int r = 0; r < 5 && ok; r++) {
+            if (r >= 2) cudaEventRecord(e0, main);
+            uw_status s = uw_sequence_run(steps, n, B, ws, ws_bytes, stream, side_stream, d);
+            if (s != UW_OK) {
+                if (d == 0) result = s;
+                ok = false;
+                break;
+            }
+            if (r >= 2) {
+                cudaEventRecord(e1, main);
+                if (cudaEventSynchronize(e1) != cudaSuccess) { ok = false; break; }
+                cudaEventElapsedTime(&t[r - 2], e0, e1);
+            }
+        }
+        if (!ok) {
+            if (result != UW_OK) break;
+            continue;
+        }
+        std::sort(t, t + 3);
+        if (t[1] < best * 0.99f) { best = t[1]; *decode_sms = d; }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return result;
+}
