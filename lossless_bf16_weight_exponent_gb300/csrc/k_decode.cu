@@ -8,9 +8,13 @@
 //
 // Palette decode: one thread per 16 weights (16-byte sign+mantissa load, 8-byte
 // code load), one verbatim test per 16 weights (a 64-weight block never splits).
-// Huffman decode: one thread per chunk of C weights, 64-bit bit buffer, a
-// 2^L-entry decode table in shared memory; a stream that does not end exactly at
-// its chunk's end offset, or hits an unassigned prefix, latches DEV_CORRUPT.
+// Huffman decode: one thread per chunk of C weights, 64-bit bit buffer, a decode
+// table in shared memory.  With a length limit of at most 12 a 12-bit
+// multi-symbol table gives up to five codes per lookup and each block's four
+// groups of 16 codes are decoded one group at a time (a group's lookups run in a
+// tight loop, its output leaves in one store); longer limits take one symbol
+// per lookup.  A stream that does not end exactly at its chunk's end offset, or
+// hits an unassigned prefix, latches DEV_CORRUPT.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -150,6 +154,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
     for (int i = threadIdx.x; i < 256; i += blockDim.x)
         pal2[i] = (uint16_t)(v.palette[i & 15] | (v.palette[i >> 4] << 8));
     __syncthreads();
+    // an entry of 0 (these 12 bits start no code) is read as one 1-bit code 0 with bit 31 set: the decode loop
+    // needs no test, and the flag is collected and reported after it
+    if (multi)
+        for (int i = threadIdx.x; i < 4096; i += blockDim.x)
+            if (mt[i] == 0u) mt[i] = 0x80000000u | (1u << 7) | (1u << 4) | 1u;
+    __syncthreads();
     // a persistent grid (fewer CTAs than groups of kDecThreads chunks, when it is given a share of the SMs) walks
     // the groups with a stride
     for (uint64_t c_first = (uint64_t)blockIdx.x * kDecThreads; c_first < v.n_chunks;
@@ -188,6 +198,134 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
     const uint32_t budget = pos1 - pos0;
     bool bad = false;
 
+    // write verbatim block b (its exponents from the verbatim section; 4-bit codes: zeros)
+    auto write_verbatim = [&](uint64_t b, uint32_t bw) {
+        const uint4 *ve = (const uint4 *)(v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64);
+        if (OUT == DEC_CODES) {
+            uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
+            o[0] = make_uint4(0, 0, 0, 0);
+            o[1] = make_uint4(0, 0, 0, 0);
+        } else if (OUT == DEC_EXP) {
+            uint4 *o = (uint4 *)((uint8_t *)out + b * 64);
+#pragma unroll
+            for (int q = 0; q < 4; q++) o[q] = ve[q];
+        } else {
+            uint4 *o = (uint4 *)((uint16_t *)out + b * 64);
+            const uint4 *sp = (const uint4 *)(v.sm + b * 64);
+#pragma unroll
+            for (int q = 0; q < 4; q++) store_bf16x16(o + 2 * q, sp[q], ve[q]);
+        }
+    };
+
+    if (multi) {
+        // the chunk's coded blocks take its symbols in order; count them first
+        uint32_t nverb = 0;
+        for (uint64_t wb = b0 >> 5; wb <= (b1 - 1) >> 5 && b1 > b0; wb++) {
+            uint32_t w = __ldg(v.bitmap + wb);
+            const uint64_t lo = wb * 32;
+            if (b0 > lo) w &= ~0u << (uint32_t)(b0 - lo);
+            if (b1 < lo + 32) w &= (1u << (uint32_t)(b1 - lo)) - 1u;
+            nverb += __popc(w);
+        }
+        int remaining = 64 * ((int)(b1 - b0) - (int)nverb);  // codes of the chunk not yet decoded
+        uint32_t bad_bits = 0;  // bit 31: a lookup met bits that start no code
+        uint64_t cacc = 0;      // decoded codes not yet used, 4 bits each, the first in the low nibble
+        uint32_t sh = 0;        // 4 x the number of codes in cacc
+        uint32_t bw = 0;
+        uint64_t bw_at = ~0ull;
+        for (uint64_t b = b0; b < b1; b++) {
+            if ((b >> 5) != bw_at) {
+                bw_at = b >> 5;
+                bw = __ldg(v.bitmap + bw_at);
+            }
+            if ((bw >> (b & 31)) & 1u) {
+                write_verbatim(b, bw);
+                continue;
+            }
+            uint64_t cw[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                uint32_t last_syms = 0, last_sh = 60;
+                // one lookup: up to five codes (one when `single`), `len` bits
+                auto lookup = [&](bool single) {
+                    const uint32_t e = mt[(uint32_t)(buf >> 52)];
+                    bad_bits |= e;
+                    const uint32_t len = single ? (e >> 7) & 15u : e & 15u;
+                    buf <<= len;
+                    avail -= (int)len;
+                    last_syms = single ? (e >> 11) & 15u : e >> 11;
+                    last_sh = sh;
+                    cacc |= (uint64_t)last_syms << sh;
+                    sh += single ? 4u : (e >> 2) & 28u;
+                };
+                if (remaining >= 21) {
+                    // more codes left than this group can take (16, plus at most 4 carried in or out): every
+                    // lookup may decode five; a refill leaves more than 32 bits, enough for two lookups
+                    const uint32_t sh0 = sh;
+                    while (sh < 64) {
+                        if (avail <= 32) {
+                            buf |= (uint64_t)nxt << (32 - avail);
+                            avail += 32;
+                            nxt = word_at(wi++);
+                        }
+                        lookup(false);
+                        if (sh >= 64) break;
+                        lookup(false);
+                    }
+                    remaining -= (int)((sh - sh0) >> 2);
+                } else {
+                    // the chunk's last coded group: its last four codes one lookup each, so no lookup takes a code
+                    // past the chunk's end
+                    while (sh < 64) {
+                        if (avail <= 32) {
+                            buf |= (uint64_t)nxt << (32 - avail);
+                            avail += 32;
+                            nxt = word_at(wi++);
+                        }
+                        const uint32_t sh0 = sh;
+                        lookup(remaining < 5);
+                        remaining -= (int)((sh - sh0) >> 2);
+                    }
+                }
+                cw[q] = cacc;
+                // codes of the last lookup beyond the 16th stay for the next group (last_sh >= 44 here)
+                cacc = (uint64_t)(last_syms >> (64u - last_sh));
+                sh -= 64;
+                if (remaining < 0) break;  // a corrupt stream: the end check below reports it
+            }
+            if (remaining < 0) {
+                bad = true;
+                break;
+            }
+            if (OUT == DEC_CODES) {
+                uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
+                o[0] = make_uint4((uint32_t)cw[0], (uint32_t)(cw[0] >> 32), (uint32_t)cw[1], (uint32_t)(cw[1] >> 32));
+                o[1] = make_uint4((uint32_t)cw[2], (uint32_t)(cw[2] >> 32), (uint32_t)cw[3], (uint32_t)(cw[3] >> 32));
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    uint32_t e[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t cb = (uint32_t)(cw[q] >> (16 * i));
+                        e[i] = (uint32_t)pal2[cb & 0xFF] | ((uint32_t)pal2[cb >> 8 & 0xFF] << 16);
+                    }
+                    const uint4 ev = make_uint4(e[0], e[1], e[2], e[3]);
+                    if (OUT == DEC_EXP) *(uint4 *)((uint8_t *)out + b * 64 + q * 16) = ev;
+                    else {
+                        const uint4 sv = *(const uint4 *)(v.sm + b * 64 + q * 16);
+                        store_bf16x16((uint4 *)((uint16_t *)out + b * 64 + q * 16), sv, ev);
+                    }
+                }
+            }
+        }
+        // every code of the chunk was used, no code started on unassigned bits, and the codes ended exactly at the
+        // next chunk's offset
+        const uint64_t at = 32ull * (wi - 1) - (uint64_t)avail;
+        if (bad || (bad_bits >> 31) || sh != 0 || at != (uint64_t)pos1) atomicExch(v.status, (int)DEV_CORRUPT);
+        continue;
+    }
+
     // emit 16 codes (one u64 word) of non-verbatim block b, quarter q
     auto emit = [&](uint64_t b, int q, uint64_t cw) {
         if (OUT == DEC_CODES) {
@@ -219,22 +357,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
         // verbatim blocks are written here directly
         for (uint32_t m = vmask; m; m &= m - 1) {
             const uint64_t b = bs + (uint64_t)(__ffs(m) - 1);
-            const uint32_t bw = __ldg(v.bitmap + (b >> 5));
-            const uint4 *ve = (const uint4 *)(v.verb_exp + (uint64_t)(__ldg(v.prefix + (b >> 5)) + __popc(bw & ((1u << (b & 31)) - 1u))) * 64);
-            if (OUT == DEC_CODES) {
-                uint4 *o = (uint4 *)((uint8_t *)out + b * 32);
-                o[0] = make_uint4(0, 0, 0, 0);
-                o[1] = make_uint4(0, 0, 0, 0);
-            } else if (OUT == DEC_EXP) {
-                uint4 *o = (uint4 *)((uint8_t *)out + b * 64);
-#pragma unroll
-                for (int q = 0; q < 4; q++) o[q] = ve[q];
-            } else {
-                uint4 *o = (uint4 *)((uint16_t *)out + b * 64);
-                const uint4 *sp = (const uint4 *)(v.sm + b * 64);
-#pragma unroll
-                for (int q = 0; q < 4; q++) store_bf16x16(o + 2 * q, sp[q], ve[q]);
-            }
+            write_verbatim(b, __ldg(v.bitmap + (b >> 5)));
         }
         // the non-verbatim blocks of the group take the group's symbols in order, 16 codes per output word
         uint32_t rem = ~vmask & ((1u << nb) - 1u);
@@ -266,28 +389,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_huffman_kernel(DevView v, 
                 nxt = word_at(wi++);
             }
         };
-        if (multi) {
-            while (produced + 5 <= total) {
-                const uint32_t e = mt[(uint32_t)(buf >> 52)];
-                uint32_t len = e & 15u;
-                int cnt = (int)((e >> 4) & 7u);
-                if (len == 0) { bad = true; len = 1; cnt = 1; }
-                advance(len);
-                put(e >> 11, cnt);
-                produced += cnt;
-            }
-        }
+        // (limits above 12 bits: one symbol per lookup of the 2^L-entry table)
         while (produced < total) {
-            uint32_t len, sym;
-            if (multi) {
-                const uint32_t e = mt[(uint32_t)(buf >> 52)];
-                len = (e >> 7) & 15u;
-                sym = (e >> 11) & 15u;
-            } else {
-                const uint32_t e = dt[(uint32_t)(buf >> (64 - L))];
-                len = e & 15u;
-                sym = e >> 4;
-            }
+            const uint32_t e = dt[(uint32_t)(buf >> (64 - L))];
+            uint32_t len = e & 15u;
+            const uint32_t sym = e >> 4;
             if (len == 0) { bad = true; len = 1; }
             advance(len);
             put(sym, 1);

@@ -37,6 +37,22 @@ def test_decode_bit_exact(name, make, codec, chunk, L):
     assert np.array_equal(got, w)
 
 
+@pytest.mark.parametrize("chunk,L", [(256, 12), (64, 5), (512, 15), (2048, 12)])
+@pytest.mark.parametrize("name,make", list(_cases()), ids=[c[0] for c in _cases()])
+def test_transcoded_palette_form_bit_exact(name, make, chunk, L):
+    # the load-time transcode (Huffman stream -> 4-bit codes, the palette-transcode preprocess) must give codes
+    # that decode to the original bits; the stream is dropped, so every later read goes through those codes
+    t = torch()
+    w = make()
+    blob = uw.encode(w, uw.CODEC_HUFFMAN, chunk, L)
+    m = uw.Matrix(blob, resident="palette")
+    assert not m.info["has_huffman_stream"]
+    out = t.empty(w.shape, dtype=t.int16, device="cuda")
+    m.decode(out)
+    m.check()
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), w)
+
+
 @pytest.mark.parametrize("codec", [0, 1])
 def test_decode_full_size_gate_8b(codec):
     t = torch()
