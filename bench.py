@@ -435,9 +435,10 @@ def measure_workload(cfg, mat, batches, resident, stream, hbm, tf_peak, blob=Non
 def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)):
     """The 8B MLP stack: gate, up, down per layer (per-layer seeds), one graph per pass over all 3 x layers
     matmuls.  All layers easy (palette form resident, AUTO: direct palette); then hard layers (the Huffman stream
-    alone, transcoded on a side stream into double-buffered slots by uw_sequence_run) every k-th layer; then every
-    matrix as the Huffman stream alone under AUTO (the Huffman-direct GEMV up to B = 8).  The gate/up shape and the
-    down shape are autotuned once each per form and the tables shared by shape."""
+    alone) every k-th layer, run by uw_sequence_run under the schedule uw_sequence_tune picks: a side-stream
+    transcode into double-buffered slots (with a decode SM split) or the direct schedule (each hard step's own AUTO
+    plan, the Huffman-direct GEMV up to B = 8); then every matrix as the Huffman stream alone under AUTO.  The
+    gate/up shape and the down shape are autotuned once each per form and the tables shared by shape."""
     import torch
 
     import lossless_bf16_weight_exponent_gb300 as uw
@@ -481,7 +482,8 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
             hard = sum(1 for m in mats if not m.info["has_palette_form"])
             d = uw.sequence_tune(steps, B, wsp, need, stream, side) if hard else 0  # the decode-vs-matmul SM split
             us = time_graph(lambda i, s: uw.sequence_run(steps, B, wsp, need, s, side, d), 1, 5, stream)
-            resident = sum(m.info["device_bytes"] for m in mats) + (need if hard else 0)
+            # the transcode slots are resident while the sequence runs; the direct schedule uses none
+            resident = sum(m.info["device_bytes"] for m in mats) + (need if hard and d != uw.SEQ_DIRECT else 0)
             base_us = base_us or us
             comp = sum(algorithmic_bytes(m.info, 4 if m.info["has_palette_form"] else 3, B) for m in mats)
             out.append(point_line("stack_8b", f"{layers} layers x (gate, up W[14336,4096]; down W[4096,14336])", B,
@@ -489,9 +491,11 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
                                   {"gate_up": pal[0].plan_for(B).as_tuple(), "down": pal[2].plan_for(B).as_tuple()},
                                   hbm, tf_peak,
                                   {"schedule": name, "matmuls": len(mats), "hard_matmuls": hard, "decode_sms": d,
+                                   "hard_steps": ("none" if not hard else "Huffman-direct (direct schedule)"
+                                                  if d == uw.SEQ_DIRECT else "side-stream transcode"),
                                    "us_per_matmul": round(us / len(mats), 2), "time_vs_all_easy": round(us / base_us, 3),
                                    "resident_ratio": round(resident / bf16_bytes, 4),
-                                   "api": "uw_sequence_run (hard steps transcoded on a side stream)"}))
+                                   "api": "uw_sequence_run, schedule from uw_sequence_tune"}))
             del wsb
         # every matrix as the Huffman stream alone, AUTO plan per call
         if B <= 8:

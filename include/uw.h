@@ -347,17 +347,20 @@ typedef struct {
  */
 /*   decode_sms: the post's decode-vs-matmul SM split.  0: every launch sizes its grid for all SMs.  d > 0: the
  *   main stream's persistent matmul grids are sized for the device's SMs minus d, and each transcode is a
- *   persistent grid of d SMs' worth of CTAs, so the two run side by side.  Must lie in [0, SMs).
+ *   persistent grid of d SMs' worth of CTAs, so the two run side by side.  UW_SEQ_DIRECT (-1): no side-stream
+ *   transcode; every step runs its own AUTO plan on `stream` (a hard step at B <= 8: the Huffman-direct GEMV;
+ *   `side_stream` is not used).  Must lie in [-1, SMs).
  */
+#define UW_SEQ_DIRECT (-1)
 uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int64_t B, size_t *bytes);
 uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
                           uw_stream side_stream, int decode_sms);
 
 /*
- * uw_sequence_tune - time uw_sequence_run over these steps (same arguments) for a range of decode SM splits
- *   (0, 8, 16, ..., 96; CUDA events on `stream`, median of three runs after two) and return the fastest split in
- *   *decode_sms (the post's tuning of the decoder's share of the SMs).  Synchronous; runs the sequence 5 times per
- *   split, writing the steps' outputs.
+ * uw_sequence_tune - time uw_sequence_run over these steps (same arguments) for the direct schedule and a range of
+ *   decode SM splits (UW_SEQ_DIRECT, 0, 8, 16, ..., 96; CUDA events on `stream`, median of three runs after two)
+ *   and return the fastest in *decode_sms (the post's tuning of the decoder's share of the SMs).  Synchronous;
+ *   runs the sequence 5 times per candidate, writing the steps' outputs.
  */
 uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
                            uw_stream side_stream, int *decode_sms);

@@ -29,6 +29,7 @@ OUT_F32, OUT_BF16 = 0, 1
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_TC = 0, 1, 2
 RESIDENT_HUFFMAN, RESIDENT_BOTH, RESIDENT_PALETTE = 0, 1, 2
 RESIDENT = {"huffman": RESIDENT_HUFFMAN, "both": RESIDENT_BOTH, "palette": RESIDENT_PALETTE}
+SEQ_DIRECT = -1  # uw_sequence_run schedule: no side-stream transcode, every step its own AUTO plan
 
 
 class UwError(RuntimeError):
@@ -291,7 +292,7 @@ def sequence_workspace_size(steps, B: int) -> int:
 
 def sequence_run(steps, B: int, workspace, ws_bytes: int, stream=None, side_stream=None, decode_sms: int = 0):
     """uw_sequence_run: the steps in order on `stream`, hard steps' transcodes on `side_stream` (on `decode_sms`
-    SMs beside the matmuls when it is > 0)."""
+    SMs beside the matmuls when it is > 0; SEQ_DIRECT: no transcode, every step its own AUTO plan)."""
     _check(lib().uw_sequence_run(_steps(steps), len(steps), B, _ptr(workspace), ws_bytes, _stream(stream),
                                  _stream(side_stream), decode_sms), "uw_sequence_run")
 

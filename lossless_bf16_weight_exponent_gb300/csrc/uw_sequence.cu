@@ -13,8 +13,11 @@
 // The section on the decode kernels adds that the decoder and the matmul cannot share an SM on H100 (the matmul's
 // shared memory leaves no room for the decoder's table), so the SMs are split between them and the split is tuned.
 // Here `decode_sms` d > 0 sizes the main stream's persistent matmul grids for the device's SMs minus d and gives the
-// transcode a persistent grid of d SMs' worth of CTAs, so the two run side by side; uw_sequence_tune times a
-// range of d and returns the fastest.
+// transcode a persistent grid of d SMs' worth of CTAs, so the two run side by side; d = UW_SEQ_DIRECT (-1) runs
+// no transcode at all: every step, hard or easy, takes its own AUTO plan on the main stream (for a hard step at
+// batch 8 or less, the GEMV that decodes the Huffman stream inside the product).  uw_sequence_tune times these
+// schedules and returns the fastest: when a matmul already holds HBM at its peak, a transcode beside it cannot
+// hide, and decoding inside the product costs less than transcoding first.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -51,6 +54,11 @@ uw_status layout_of(const uw_step *steps, int n, int64_t B, Layout *L)
             L->hard++;
             L->slot = std::max(L->slot, slot_bytes_of(m));
             L->mm = std::max<uint64_t>(L->mm, round_up(matmul_with_codes_workspace(m, B), 256));
+            // the direct schedule runs the step's own AUTO plan instead
+            size_t b = 0;
+            uw_status s = uw_workspace_size(m, B, UW_STRAT_AUTO, &b);
+            if (s != UW_OK) return s;
+            L->mm = std::max<uint64_t>(L->mm, round_up(b, 256));
         } else {
             size_t b = 0;
             uw_status s = uw_workspace_size(m, B, UW_STRAT_AUTO, &b);
@@ -104,8 +112,8 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
 {
     clear_error();
     if (n < 0 || (n && !steps) || B < 0) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: bad arguments");
-    if (decode_sms < 0 || decode_sms >= device_sms())
-        return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: decode_sms %d outside [0, %d)", decode_sms, device_sms());
+    if (decode_sms < UW_SEQ_DIRECT || decode_sms >= device_sms())
+        return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: decode_sms %d outside [-1, %d)", decode_sms, device_sms());
     if (n == 0 || B == 0) return UW_OK;
     Layout L;
     uw_status s = layout_of(steps, n, B, &L);
@@ -113,7 +121,7 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
     const uint64_t need = (L.hard ? 2 * L.slot : 0) + L.mm;
     if (ws_bytes < need || (need && !ws)) return fail(UW_ERR_WORKSPACE, "uw_sequence_run: workspace %zu bytes, need %llu", ws_bytes, (unsigned long long)need);
     if (ws && ((uintptr_t)ws & 255)) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: workspace not 256-byte aligned");
-    if (L.hard && (stream == side_stream))
+    if (L.hard && decode_sms != UW_SEQ_DIRECT && stream == side_stream)
         return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: the side stream must differ from the main stream");
     for (int i = 0; i < n; i++)
         if (steps[i].out_dtype != UW_OUT_F32 && steps[i].out_dtype != UW_OUT_BF16)
@@ -122,7 +130,7 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
     uint8_t *mm = (uint8_t *)ws + (L.hard ? 2 * L.slot : 0);
     cudaStream_t main = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
 
-    if (!L.hard) {
+    if (!L.hard || decode_sms == UW_SEQ_DIRECT) {
         for (int i = 0; i < n; i++) {
             s = uw_matmul(steps[i].m, steps[i].x, B, steps[i].y, (uw_out_dtype)steps[i].out_dtype, UW_STRAT_AUTO, mm, L.mm,
                           stream);
@@ -192,7 +200,7 @@ extern "C" uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, vo
     const int sms = device_sms();
     float best = 3.0e38f;
     uw_status result = UW_OK;
-    for (int d : {0, 8, 16, 24, 32, 40, 48, 64, 80, 96}) {
+    for (int d : {UW_SEQ_DIRECT, 0, 8, 16, 24, 32, 40, 48, 64, 80, 96}) {
         if (d >= sms) continue;
         float t[3];
         bool ok = true;

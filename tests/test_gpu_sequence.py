@@ -41,7 +41,7 @@ def _run(mats, ws, B, out_dtype, graph=False, decode_sms=0, tune=False):
     main, side = t.cuda.Stream(), t.cuda.Stream()
     if tune:
         decode_sms = uw.sequence_tune(steps, B, wsp, need, main, side)
-        assert decode_sms in (0, 8, 16, 24, 32, 40, 48, 64, 80, 96)
+        assert decode_sms in (uw.SEQ_DIRECT, 0, 8, 16, 24, 32, 40, 48, 64, 80, 96)
         t.cuda.synchronize()
         for y in ys:
             y.fill_(float("nan"))
@@ -73,7 +73,7 @@ def test_sequence_matches_the_oracle(stack, hard_layers, B):
 
 
 @pytest.mark.parametrize("hard_layers", [(1, 3), (0, 1, 2, 3)])
-@pytest.mark.parametrize("decode_sms", [0, 40])
+@pytest.mark.parametrize("decode_sms", [0, 40, uw.SEQ_DIRECT])
 def test_sequence_in_a_cuda_graph_and_bf16(stack, hard_layers, decode_sms):
     ws, blobs = stack
     _run(_mats(blobs, set(hard_layers)), ws, 3, uw.OUT_BF16, graph=True, decode_sms=decode_sms)
@@ -83,7 +83,7 @@ def test_sequence_in_a_cuda_graph_and_bf16(stack, hard_layers, decode_sms):
 def test_sequence_with_a_decode_split(stack, B):
     # the matmuls' grids sized for the SMs left beside the transcode: same results; and the tuner's choice
     ws, blobs = stack
-    for d in (8, 76, 151):
+    for d in (8, 76, 151, uw.SEQ_DIRECT):
         _run(_mats(blobs, {0, 2}), ws, B, uw.OUT_F32, decode_sms=d)
     _run(_mats(blobs, {1, 2}), ws, B, uw.OUT_F32, tune=True)
 
@@ -109,4 +109,8 @@ def test_sequence_workspace_and_argument_errors(stack):
     with pytest.raises(uw.UwError) as e:  # the split must leave the matmuls at least one SM
         uw.sequence_run(steps, 1, p, need, s, t.cuda.Stream(), 100000)
     assert e.value.status == uw.ERR_INVALID_ARG
+    with pytest.raises(uw.UwError) as e:  # below the direct schedule
+        uw.sequence_run(steps, 1, p, need, s, t.cuda.Stream(), -2)
+    assert e.value.status == uw.ERR_INVALID_ARG
+    uw.sequence_run(steps, 1, p, need, s, s, uw.SEQ_DIRECT)  # no transcode: one stream is enough
     uw.sequence_run([], 1, None, 0, s, s)  # nothing to run
