@@ -287,8 +287,9 @@ uw_status uw_matmul_host_async(const uw_matrix *m, const uint16_t *x_host, int64
  *   one array and it keeps the last call's contents (the accumulator is
  *   cleared on the stream before each use): calls whose GPU work overlaps
  *   (different streams, or different threads without ordering) race on it.
- *   Errors: UW_ERR_WORKSPACE when N*K/2 plus B*N*4 (each rounded up to 256
- *   bytes, with 64 bytes of padding on the codes) exceeds the 36 MiB array;
+ *   Errors: UW_ERR_WORKSPACE when N*K/2 plus B*N*4 plus 24 bytes per 128 rows
+ *   (each rounded up to 256 bytes, with 64 bytes of padding on the codes)
+ *   exceeds the 36 MiB array;
  *   UW_ERR_UNSUPPORTED for a palette-codec matrix; otherwise as uw_matmul.
  */
 uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev, int64_t B, void *y_dev, uw_out_dtype out_dtype,

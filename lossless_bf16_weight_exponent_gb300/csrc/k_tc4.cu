@@ -18,7 +18,15 @@
 //   - warp 18 (one thread) issues per step four tcgen05.mma (M = 128, N = BN <= 256, K = 16; two per K-slice
 //     above 256) from the A tile and the X tile into the tensor-memory accumulator of the current segment (a run
 //     of units of one row block); two accumulator buffers when they fit;
-//   - warps 19-26 write a finished segment: tcgen05.ld, fp32 atomic adds into a target zeroed just before.
+//   - warps 19-26 write a finished segment.  A segment that covers its whole row block (every unit of K) is
+//     stored at once (fp32, or rounded to bf16).  A row block shared by several CTAs is combined through two
+//     cells of the workspace tagged with the launch's epoch, so they need no zeroing.  The CTA whose range
+//     starts inside the block has the block's last units as its first segment and finishes its share early:
+//     it stores the share and raises the block's flag.  The others (the block's first units end their
+//     ranges) wait for the flag and add theirs with fp32 atomics.  With two sharers and fp32 output the adder
+//     then clears the flag; otherwise the adders count themselves, and the last rounds the block to bf16 when
+//     that is the output and clears the cells.  No kernel zeroes the target first, so nothing waits on a
+//     zeroing pass between launches.
 // Every wait is bounded; on expiry the kernel latches DEV_TIMEOUT, drains its copies and MMAs and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -26,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "dev_async.cuh"
@@ -60,13 +69,23 @@ constexpr size_t kSmemCap = 227 * 1024;
 static_assert(kVOff + 64 + kVCs * 64 <= kWStage, "weight stage layout");
 static_assert((2 * kMaxSW + 2 * kMaxSX + 2 * kMaxSA + 5) * 8 + 4 <= kBarBytes, "barrier region");
 
+// the workspace cells of one 128-row tile: the adders' count ((epoch << 24) | count) and the flag (the epoch,
+// once the storing CTA's sums are visible); the third is spare
+struct TileCells {
+    unsigned long long done, flag, spare;
+};
+
 struct Tc4Args {
     CUtensorMap tm_sm;     // sm [N, K] u8, box {64, 128}, dense
     CUtensorMap tm_codes;  // codes [N, K/2] u8, box {32, 128}, dense
     CUtensorMap tm_x;      // X [B, K] bf16, box {64, min(BN, 256)}, 128-byte swizzle
     const uint32_t *tmv_off, *tmv_mask;
     const uint8_t *tmv_data;
-    float *acc;            // [B, N] fp32, zeroed before the launch
+    void *y;               // [B, N] fp32 or bf16
+    float *acc;            // [B, N] fp32 workspace rows of the shared row blocks (bf16 output only)
+    TileCells *cells;      // one per 128-row tile
+    unsigned long long epoch;  // this launch's tag (40 bits, never 0)
+    int out_bf16;
     int *status;
     int64_t N, B, units;
     int upk, BN, SW, SX, SA, nbuf, buf_stride, tmem_cols, w_from_prev;
@@ -118,6 +137,33 @@ __device__ __forceinline__ void fill_pair_table16(uint8_t *tab, const uint8_t *p
         *(uint4 *)(tab + 64 * b + 16 * q) = make_uint4(v, v, v, v);
     }
 }
+
+// count one more in a tagged cell of this epoch (a cell of another epoch counts as 0); returns the count before
+__device__ __forceinline__ uint32_t tagged_count(unsigned long long *cell, unsigned long long epoch)
+{
+    unsigned long long cur = *(volatile unsigned long long *)cell;
+    for (;;) {
+        const unsigned long long nxt = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
+        const unsigned long long prev = atomicCAS(cell, cur, nxt);
+        if (prev == cur) return (uint32_t)(nxt & 0xFFFFFFu) - 1u;
+        cur = prev;
+    }
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// the CTA holding unit u of a balanced partition of U units over G CTAs (u0(b) = U b / G)
+__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t G) { return ((u + 1) * G - 1) / U; }
 
 __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant__ Tc4Args a)
 {
@@ -362,9 +408,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
         if (!ok) atomicExch(a.status, (int)DEV_TIMEOUT);
     } else {
         // ---------------------------------------------------------------------------------------- epilogue
-        grid_dependency_wait();  // the target is zeroed by the preceding kernel
+        grid_dependency_wait();  // Y and the workspace may belong to the preceding kernel
         const int q = warp & 3, half = (warp - kEpiWarp0) >> 2;
+        const int et = threadIdx.x - 32 * kEpiWarp0;  // 0 .. 255 over the epilogue warps
+        const bool lead = et == 0;
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        volatile uint32_t *bcast = tmem_slot + 1;  // the lead thread's word to the other epilogue threads
+        auto epi_sync = [] { asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory"); };
         int64_t tile = u0 / upk;
         int kq = (int)(u0 % upk), seg = 0;
         for (int cu = 0; cu < nu; cu++) {
@@ -376,20 +426,85 @@ __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant_
             const bool got = mbar_wait(&accfull[buf], (seg / a.nbuf) & 1);
             if (!got) atomicExch(a.status, (int)DEV_TIMEOUT);
             tc_fence_after();
+            // the CTAs that share the row block: one of them (whole) or several (combined through its cells); the
+            // one holding the block's last unit starts its range inside the block and stores its share
+            const int64_t b_lo = cta_of_unit(t_cur * upk, U, G), b_hi = cta_of_unit(t_cur * upk + upk - 1, U, G);
+            const bool whole = b_lo == b_hi;
+            const bool storer = !whole && (int64_t)blockIdx.x == b_hi;
+            const bool counted = !whole && (a.out_bf16 || b_hi - b_lo >= 2);  // adders count themselves
+            TileCells *cell = a.cells + t_cur;
+            if (!whole && !storer) {
+                if (lead) {
+                    // the stored share must be visible before this one is added (bounded wait)
+                    const uint64_t t0 = gtime();
+                    while (ld_acquire(&cell->flag) != a.epoch)
+                        if (gtime() - t0 > kWaitLimitNs) {
+                            atomicExch(a.status, (int)DEV_TIMEOUT);
+                            break;
+                        }
+                }
+                epi_sync();
+            }
             const int64_t row = t_cur * kRows + 32 * q + lane;
+            float *tf = a.out_bf16 ? a.acc : (float *)a.y;  // where a shared block's sums meet
             for (int c0 = 16 * half; c0 < a.B; c0 += 32) {
                 uint32_t v[16];
                 tmem_ld16(tmem + t_lane + (uint32_t)(buf * a.buf_stride + c0), v);
                 tmem_wait_ld();
-                if (got && row < a.N) {
+                if (row < a.N) {
 #pragma unroll
-                    for (int e = 0; e < 16; e++)
-                        if (c0 + e < a.B) atomicAdd(a.acc + (int64_t)(c0 + e) * a.N + row, __uint_as_float(v[e]));
+                    for (int e = 0; e < 16; e++) {
+                        if (c0 + e >= a.B) break;
+                        const int64_t o = (int64_t)(c0 + e) * a.N + row;
+                        const float f = __uint_as_float(v[e]);
+                        if (whole) {
+                            if (a.out_bf16) ((__nv_bfloat16 *)a.y)[o] = __float2bfloat16_rn(f);
+                            else ((float *)a.y)[o] = f;
+                        } else if (storer) {
+                            tf[o] = f;
+                        } else {
+                            atomicAdd(tf + o, f);
+                        }
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&accempty[buf]);
+            if (storer) {
+                // the share is visible at gpu scope before the flag
+                __threadfence();
+                epi_sync();
+                if (lead) st_release(&cell->flag, a.epoch);
+            } else if (!whole && !counted) {
+                // the only adder: the flag goes back to no epoch (a CUDA graph replays this launch with the same one)
+                if (lead) cell->flag = 0ull;
+            } else if (counted) {
+                __threadfence();
+                epi_sync();
+                if (lead) {
+                    const uint32_t d = tagged_count(&cell->done, a.epoch);
+                    __threadfence();
+                    *bcast = d + 1 == (uint32_t)(b_hi - b_lo) ? 1u : 0u;
+                }
+                epi_sync();
+                if (*bcast) {
+                    // the block's last adder: every share is in
+                    __threadfence();
+                    if (a.out_bf16) {
+                        for (int i = et; i < kRows * (int)a.B; i += 32 * kEpiWarps) {
+                            const int64_t rr = t_cur * kRows + (i % kRows);
+                            const int64_t o = (int64_t)(i / kRows) * a.N + rr;
+                            if (rr < a.N) ((__nv_bfloat16 *)a.y)[o] = __float2bfloat16_rn(__ldcg(a.acc + o));
+                        }
+                    }
+                    if (lead) {
+                        cell->done = 0ull;
+                        cell->flag = 0ull;
+                    }
+                }
+                epi_sync();  // the broadcast word is free again
+            }
             seg++;
         }
     }
@@ -486,11 +601,17 @@ int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
     a.tmem_cols = s.tmem_cols;
     a.w_from_prev = w.w_from_prev;
     memcpy(a.palette, w.palette, 16);
-    // a row block's partial sums may come from two CTAs: both add into a zeroed fp32 target
-    a.acc = out_bf16 ? acc_ws : (float *)y;
-    if (!a.acc || ((uintptr_t)a.acc & 15)) return cudaErrorInvalidValue;
-    cudaError_t e = (cudaError_t)launch_zero_target(a.acc, B * w.N, st);
-    if (e != cudaSuccess) return e;
+    // a row block shared by several CTAs meets in Y (fp32) or in the workspace's accumulator (bf16), through its
+    // cells after the accumulator region; nothing needs zeroing
+    if (!acc_ws || ((uintptr_t)acc_ws & 15) || !y || ((uintptr_t)y & 15)) return cudaErrorInvalidValue;
+    a.y = y;
+    a.acc = acc_ws;
+    a.cells = (TileCells *)((uint8_t *)acc_ws + acc_region_bytes(B, w.N));
+    a.out_bf16 = out_bf16;
+    static std::atomic<unsigned long long> launches{0};
+    do a.epoch = (launches.fetch_add(1) + 1) & ((1ull << 40) - 1);
+    while (!a.epoch);
+    cudaError_t e = cudaSuccess;
     static bool attr = false;
     if (!attr) {
         e = cudaFuncSetAttribute(tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCap);
@@ -507,10 +628,7 @@ int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
     la[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = la;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, tc4_kernel, a);
-    if (e != cudaSuccess) return e;
-    if (out_bf16) return launch_finalize(acc_ws, y, B * w.N, 1, stream);
-    return cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, tc4_kernel, a);
 }
 
 }  // namespace uw

@@ -125,9 +125,14 @@ int launch_gemv_huff(const DevView &v, const uint16_t *x, int64_t B, void *y, in
 // preceding kernel before writing and lets the following matmul start at once
 int launch_zero_target(float *p, int64_t count, void *stream);
 // persistent tcgen05 GEMM with rebuilt weights in shared memory (tensor-core variant 4): B <= 512, 4-bit codes,
-// K % 256 == 0
+// K % 256 == 0.  acc_ws: the matmul workspace (the fp32 accumulator region of acc_region_bytes, then the
+// row-tile cells of tile_cells_bytes); needs no zeroing
 bool tc4_supported(const WOperand &w, int64_t B);
 int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, float *acc_ws, void *stream);
+// the matmul workspace after the preprocess output: an fp32 accumulator [B][N], then three 8-byte cells per
+// 128-row tile (a row tile's partial sums from several CTAs are combined through them)
+inline uint64_t acc_region_bytes(int64_t B, int64_t N) { return ((uint64_t)B * (uint64_t)N * 4 + 255) / 256 * 256; }
+inline uint64_t tile_cells_bytes(int64_t N) { return ((uint64_t)(N + 127) / 128 * 24 + 255) / 256 * 256; }
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);

@@ -105,7 +105,7 @@ extern "C" uw_status uw_matmul_noalloc(const uw_matrix *m, const uint16_t *x_dev
         return uw::fail(UW_ERR_INVALID_ARG, "uw_matmul_noalloc: bad output dtype");
     const uint64_t n = (uint64_t)info.N * (uint64_t)info.K;
     const uint64_t codes_bytes = round_up(n / 2 + 64, 256);
-    const uint64_t acc_bytes = round_up((uint64_t)B * (uint64_t)info.N * 4, 256);
+    const uint64_t acc_bytes = uw::acc_region_bytes(B, info.N) + uw::tile_cells_bytes(info.N);
     if (codes_bytes + acc_bytes > UW_NOALLOC_SCRATCH_BYTES)
         return uw::fail(UW_ERR_WORKSPACE,
                         "uw_matmul_noalloc: needs %llu scratch bytes (4-bit codes %llu + accumulator %llu), "

@@ -333,9 +333,10 @@ static uint64_t split_bytes(const uw_matrix *m, int64_t B, const uw_plan &p, int
     WOperand w = operand_shape(m, p.strategy);
     int split = p.split_k > 0 ? p.split_k
                               : (kernel == UW_KERNEL_TC ? tc_default_split(w, B, p.variant) : gemv_default_split(w, B));
-    // the GEMV may raise the split to fit its X slice; reserve the accumulator whenever a split is possible
+    // the GEMV may raise the split to fit its X slice; reserve the accumulator whenever a split is possible, and
+    // the row-tile cells of the tensor-core kernel
     (void)split;
-    return round_up((uint64_t)B * (uint64_t)m->h.N * 4, 256);
+    return acc_region_bytes(B, m->h.N) + tile_cells_bytes(m->h.N);
 }
 
 // the kernel and launch shape for a strategy and batch when no tuned plan exists

@@ -73,3 +73,48 @@ def test_tc_gate_8b(B):
         y = pick(run_matmul(m, x, (uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, v)), rows)
         ok, worst = tol_ok(y, yref, absum)
         assert ok, (v, worst)
+
+
+@pytest.mark.parametrize("shape", [(1000, 1024), (1024, 256), (300, 4096)])
+@pytest.mark.parametrize("B", [40, 300])
+@pytest.mark.parametrize("out_dtype", [uw.OUT_F32, uw.OUT_BF16])
+def test_tc4_shared_row_blocks_replays_and_dirty_workspace(shape, B, out_dtype):
+    # The persistent kernel combines a row block that several CTAs share through three workspace cells tagged
+    # with the launch's epoch (no zeroing): 1000 x 1024 has 32 units of 128 rows x 256 weights, one per CTA, so
+    # every row block is shared by four CTAs (and the last one is ragged); 1024 x 256 has one unit per row block
+    # (nothing shared); 300 x 4096 shares its three blocks unevenly.  The workspace starts as garbage; the same
+    # launch runs eagerly twice and then from a CUDA graph three times (a replay keeps its epoch, so the cells
+    # must be back to no epoch after every launch), each against the oracle's fp64 contraction.
+    t = __import__("uwtest").torch()
+    from uwtest import dev_bytes, to_dev_u16
+    w = synth.fill(shape, seed=shape[0] + B, scale=0.02, p1=2e-3, f1=300.0)
+    m = uw.Matrix(uw.encode(w, uw.CODEC_HUFFMAN, 256, 12), resident="palette")
+    x_np = synth.fill((B, shape[1]), seed=B + 7)
+    yref, absum = oracle.matmul(w, x_np)
+    plan = uw.Plan(uw.STRAT_DIRECT_PALETTE, uw.KERNEL_TC, 0, 4)
+    need = m.plan_workspace_size(B, plan)
+    ws = dev_bytes(need)
+    ws.fill_(0xA5)
+    x = to_dev_u16(x_np)
+    y = t.empty((B, shape[0]), dtype=t.float32 if out_dtype == uw.OUT_F32 else t.bfloat16, device="cuda")
+    s = t.cuda.Stream()
+
+    def check():
+        t.cuda.synchronize()
+        ok, worst = tol_ok(y.float().cpu().numpy().astype(np.float64), yref, absum, out_dtype == uw.OUT_BF16)
+        assert ok, worst
+        m.check()
+
+    for _ in range(2):
+        y.fill_(float("nan"))
+        m.matmul_plan(x, B, y, plan, out_dtype, ws, need, s)
+        check()
+    g = t.cuda.CUDAGraph()
+    with t.cuda.stream(s):
+        with t.cuda.graph(g, stream=s):
+            m.matmul_plan(x, B, y, plan, out_dtype, ws, need, s)
+    for _ in range(3):
+        y.fill_(float("nan"))
+        with t.cuda.stream(s):
+            g.replay()
+        check()
