@@ -48,8 +48,10 @@ constexpr int kTab = 256 * 128;            // pair table: entry b for lane l at 
 constexpr uint32_t kBoxBytes = kRows * 128;
 constexpr int kSmemCap = 227 * 1024;
 
-// verbatim blocks of a unit staged with it (beyond: global loads)
-__host__ __device__ constexpr int vc_of(int NB) { return NB == 4 ? 8 : 16; }
+// verbatim blocks of a unit staged with it (beyond: global loads); at NB = 4 four, so that the kernel leaves
+// 1 KB of the SM's shared memory to the one-warp CTA of the zeroing kernel that runs beside it
+__host__ __device__ constexpr int vc_of(int NB) { return NB == 4 ? 4 : 16; }
+constexpr int kBarArea = 64;  // the ring's full and empty barriers (at most 3 stages x 2 x 8 bytes)
 // ring stages: three up to 32 batch rows, two beyond (the X tiles grow with the batch)
 __host__ __device__ constexpr int stages_of(int NB) { return NB <= 4 ? 3 : 2; }
 __host__ __device__ constexpr int vslot_of(int NB) { return 64 + vc_of(NB) * 64; }
@@ -58,9 +60,14 @@ __host__ __device__ constexpr uint32_t stage_of(int NB) { return 3 * kBoxBytes +
 // dynamic shared memory: alignment slack, table, barriers, verbatim slots, ring
 constexpr size_t smem_of(int NB)
 {
-    return 1024 + kTab + 256 + (size_t)stages_of(NB) * (vslot_of(NB) + stage_of(NB));
+    return 1024 + kTab + kBarArea + (size_t)stages_of(NB) * (vslot_of(NB) + stage_of(NB));
 }
 static_assert(smem_of(4) <= (size_t)kSmemCap && smem_of(8) <= (size_t)kSmemCap, "shared memory of the batch shapes");
+static_assert(2 * 3 * 8 <= kBarArea, "barrier area");
+// each shape leaves room for a one-warp CTA beside it: 228 KB per SM, 1 KB reserved per CTA
+static_assert(smem_of(1) + 2048 <= 228 * 1024 && smem_of(2) + 2048 <= 228 * 1024 && smem_of(3) + 2048 <= 228 * 1024 &&
+                  smem_of(4) + 2048 <= 228 * 1024 && smem_of(6) + 2048 <= 228 * 1024 && smem_of(8) + 2048 <= 228 * 1024,
+              "room for the zeroing kernel's CTA");
 
 struct RpArgs {
     CUtensorMap tm_sm;     // sm [N, K] u8, box {128, 128}, 128-byte swizzle
@@ -135,12 +142,24 @@ __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddep
 
 // Zeroes the fp32 target of the atomic adds.  Launched as a dependent of the preceding kernel, it lets the
 // matmul that follows it start at once (streaming its weights) and zeroes only once the preceding kernel is done.
-__global__ void zero_target_kernel(float4 *p, int64_t n4, float *tail, int n_tail)
+// One warp per CTA: a CTA this small fits beside a resident matmul CTA (the matmul kernels leave it 1 KB of
+// shared memory and the registers of one warp), so every CTA of this grid starts, and lets the next matmul
+// launch, while the preceding matmul still runs.  A grid of 256-thread CTAs did not fit beside them and held
+// the next launch back until the preceding one had drained.
+constexpr int kZeroThreads = 32;
+__global__ void __launch_bounds__(kZeroThreads) zero_target_kernel(float4 *p, int64_t n4, float *tail, int n_tail)
 {
     grid_launch_dependents();
     grid_dependency_wait();
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+    const int64_t stride = (int64_t)gridDim.x * kZeroThreads;
+    int64_t i = blockIdx.x * (int64_t)kZeroThreads + threadIdx.x;
+    for (; i + 3 * stride < n4; i += 4 * stride) {
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p[i + stride] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p[i + 2 * stride] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p[i + 3 * stride] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (; i < n4; i += stride) p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (blockIdx.x == 0 && (int)threadIdx.x < n_tail) tail[threadIdx.x] = 0.f;
 }
 
@@ -158,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_rp_kernel(const __grid_const
     uint8_t *tab = ring + kStages * kStage;           // [kTab]
     uint64_t *full = (uint64_t *)(tab + kTab);        // [kStages]
     uint64_t *empty = full + kStages;                 // [kStages]
-    uint8_t *vslots = tab + kTab + 256;               // [kStages][kVSlot]: 64-byte mask, then staged blocks
+    uint8_t *vslots = tab + kTab + kBarArea;          // [kStages][kVSlot]: 64-byte mask, then staged blocks
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t U = a.units, G = gridDim.x;
@@ -396,10 +415,10 @@ cudaError_t launch_rp_nb(const RpArgs &a, int grid, cudaStream_t st)
 int launch_zero_target(float *p, int64_t n, void *stream)
 {
     const int64_t n4 = n / 4;
-    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n4 + 255) / 256, (int64_t)num_sms()));
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n4 + kZeroThreads - 1) / kZeroThreads, (int64_t)num_sms()));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(256u);
+    cfg.blockDim = dim3((unsigned)kZeroThreads);
     cfg.stream = (cudaStream_t)stream;
     cudaLaunchAttribute la[1];
     la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
