@@ -66,7 +66,7 @@ def _run(mats, ws, B, out_dtype, graph=False, decode_sms=0, tune=False):
 
 
 @pytest.mark.parametrize("hard_layers", [(), (1,), (0, 2), (0, 1, 2, 3)])
-@pytest.mark.parametrize("B", [1, 4, 20])
+@pytest.mark.parametrize("B", [1, 4, 20, 100])
 def test_sequence_matches_the_oracle(stack, hard_layers, B):
     ws, blobs = stack
     _run(_mats(blobs, set(hard_layers)), ws, B, uw.OUT_F32)
