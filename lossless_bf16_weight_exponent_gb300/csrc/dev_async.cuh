@@ -177,5 +177,42 @@ __device__ __forceinline__ uint32_t pair_exp(const uint8_t *tab_lane, uint32_t C
     return *(const uint32_t *)(tab_lane + b * 128u);
 }
 
+// ---------------------------------------------------------------------------- row blocks shared by CTAs
+// A persistent kernel over a balanced partition of row-block units stores a row block that one CTA covers and
+// combines a block that several CTAs share through three 8-byte cells of the caller's workspace, tagged with the
+// launch's epoch so that they need no zeroing: the adders' count ((epoch << 24) | count), the flag (the epoch,
+// once the storing CTA's sums are visible) and a spare.
+
+struct TileCells {
+    unsigned long long done, flag, spare;
+};
+
+// count one more in a tagged cell of this epoch (a cell of another epoch counts as 0); returns the count before
+__device__ __forceinline__ uint32_t tagged_count(unsigned long long *cell, unsigned long long epoch)
+{
+    unsigned long long cur = *(volatile unsigned long long *)cell;
+    for (;;) {
+        const unsigned long long nxt = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
+        const unsigned long long prev = atomicCAS(cell, cur, nxt);
+        if (prev == cur) return (uint32_t)(nxt & 0xFFFFFFu) - 1u;
+        cur = prev;
+    }
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// the CTA holding unit u of a balanced partition of U units over G CTAs (u0(b) = U b / G)
+__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t G) { return ((u + 1) * G - 1) / U; }
+
 }  // namespace dev
 }  // namespace uw

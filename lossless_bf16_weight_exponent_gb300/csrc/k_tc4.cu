@@ -34,7 +34,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstring>
 
 #include "dev_async.cuh"
@@ -68,12 +67,6 @@ constexpr uint32_t kBarBytes = 512;
 constexpr size_t kSmemCap = 227 * 1024;
 static_assert(kVOff + 64 + kVCs * 64 <= kWStage, "weight stage layout");
 static_assert((2 * kMaxSW + 2 * kMaxSX + 2 * kMaxSA + 5) * 8 + 4 <= kBarBytes, "barrier region");
-
-// the workspace cells of one 128-row tile: the adders' count ((epoch << 24) | count) and the flag (the epoch,
-// once the storing CTA's sums are visible); the third is spare
-struct TileCells {
-    unsigned long long done, flag, spare;
-};
 
 struct Tc4Args {
     CUtensorMap tm_sm;     // sm [N, K] u8, box {64, 128}, dense
@@ -137,33 +130,6 @@ __device__ __forceinline__ void fill_pair_table16(uint8_t *tab, const uint8_t *p
         *(uint4 *)(tab + 64 * b + 16 * q) = make_uint4(v, v, v, v);
     }
 }
-
-// count one more in a tagged cell of this epoch (a cell of another epoch counts as 0); returns the count before
-__device__ __forceinline__ uint32_t tagged_count(unsigned long long *cell, unsigned long long epoch)
-{
-    unsigned long long cur = *(volatile unsigned long long *)cell;
-    for (;;) {
-        const unsigned long long nxt = (cur >> 24) == epoch ? cur + 1 : (epoch << 24) | 1ull;
-        const unsigned long long prev = atomicCAS(cell, cur, nxt);
-        if (prev == cur) return (uint32_t)(nxt & 0xFFFFFFu) - 1u;
-        cur = prev;
-    }
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// the CTA holding unit u of a balanced partition of U units over G CTAs (u0(b) = U b / G)
-__device__ __forceinline__ int64_t cta_of_unit(int64_t u, int64_t U, int64_t G) { return ((u + 1) * G - 1) / U; }
 
 __global__ void __launch_bounds__(kThreads, 1) tc4_kernel(const __grid_constant__ Tc4Args a)
 {
@@ -610,9 +576,7 @@ int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
     a.acc = acc_ws;
     a.cells = (TileCells *)((uint8_t *)acc_ws + acc_region_bytes(B, w.N));
     a.out_bf16 = out_bf16;
-    static std::atomic<unsigned long long> launches{0};
-    do a.epoch = (launches.fetch_add(1) + 1) & ((1ull << 40) - 1);
-    while (!a.epoch);
+    a.epoch = next_launch_epoch();
     cudaError_t e = cudaSuccess;
     static bool attr = false;
     if (!attr) {

@@ -133,6 +133,9 @@ int launch_tc4(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out
 // 128-row tile (a row tile's partial sums from several CTAs are combined through them)
 inline uint64_t acc_region_bytes(int64_t B, int64_t N) { return ((uint64_t)B * (uint64_t)N * 4 + 255) / 256 * 256; }
 inline uint64_t tile_cells_bytes(int64_t N) { return ((uint64_t)(N + 127) / 128 * 24 + 255) / 256 * 256; }
+// a fresh tag for one launch that combines shared row blocks through those cells: a process-wide count in 40 bits,
+// never 0 (a CUDA graph replays a launch with the tag it was captured with)
+uint64_t next_launch_epoch();
 int launch_finalize(const float *acc, void *y, int64_t count, int out_bf16, void *stream);
 int launch_tc(const WOperand &w, const uint16_t *x, int64_t B, void *y, int out_bf16, int split_k, int variant,
               float *acc_ws, void *stream);

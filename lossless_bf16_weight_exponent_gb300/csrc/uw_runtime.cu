@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -500,6 +501,15 @@ extern "C" uw_status uw_matmul_plan(const uw_matrix *m, const uint16_t *x, int64
 }
 
 namespace uw {
+
+uint64_t next_launch_epoch()
+{
+    static std::atomic<uint64_t> launches{0};
+    uint64_t e;
+    do e = (launches.fetch_add(1) + 1) & ((1ull << 40) - 1);
+    while (!e);
+    return e;
+}
 
 size_t matmul_with_codes_workspace(const uw_matrix *m, int64_t B)
 {
