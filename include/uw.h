@@ -215,7 +215,14 @@ uw_status uw_decode(const uw_matrix *m, uint16_t *w_dev, uw_stream stream);
  * uw_workspace_size - device workspace bytes uw_matmul needs for (m, B,
  *   strategy) (AUTO: the plan AUTO would pick; an explicit strategy: that
  *   strategy with the kernel and launch shape AUTO would pair with it at this B).
- *   0 is a valid answer.
+ *   0 is a valid answer.  The workspace holds a preprocess output, an fp32
+ *   accumulator [B,N] and 24 bytes per 128 rows of W; its contents need no
+ *   initialisation (the tensor-core kernel tags the cells it shares between
+ *   its CTAs with a per-launch epoch, and clears them before it ends, so a
+ *   CUDA graph that replays the call finds them clear).  A call owns its
+ *   workspace until `stream` has passed it: calls that may overlap take
+ *   separate workspaces.  If a call ends with UW_ERR_TIMEOUT in uw_check, a
+ *   graph replay of it on the same workspace may find stale cells.
  */
 uw_status uw_workspace_size(const uw_matrix *m, int64_t B, uw_strategy strategy, size_t *bytes);
 
