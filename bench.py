@@ -323,7 +323,8 @@ def run_reference(args):
         "data": "synthetic", "config": {"workload": f"{WORKLOAD} W[14336,4096] bf16 N(0,0.02)+1e-4x100, Huffman blob",
                                          "batch": args.batch},
         "cpu_baseline": {"value": eff, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} full steps: decode of the Huffman blob + fp64 GEMV (B={args.batch})"},
+                         "sample": f"{steps} full step{'s' if steps != 1 else ''}: decode of the Huffman blob + fp64 GEMV "
+                                   f"(B={args.batch})"},
         "e2e": {"value": eff, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
