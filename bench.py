@@ -40,6 +40,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 2 ** 20
+E2E_STREAMS = 3  # independent calls in flight in the end-to-end and concurrent measurements
 WORKLOAD = "gate_8b"
 CSRC = os.path.join(ROOT, "lossless_bf16_weight_exponent_gb300", "csrc")
 
@@ -376,6 +377,56 @@ def time_graph(fn, n, reps, stream):
     return statistics.median(ts)
 
 
+def concurrent_device(mats, mat, B, K, W, stream, nstreams=E2E_STREAMS):
+    """The same K matmuls as independent calls on `nstreams` streams (call i on stream i % nstreams, each stream with
+    its own Y and workspace), forked from and joined back to `stream` inside one CUDA graph; CUDA events on `stream`
+    around a replay, after W warm-up calls and behind the 2 ms spin kernel.  On one stream each matmul's consumers
+    wait for the preceding grid to finish (its output may be their input); independent calls on several streams
+    overlap instead.  Returns milliseconds for the K calls."""
+    import torch
+
+    import lossless_bf16_weight_exponent_gb300 as uw
+    copies = len(mats)
+    side = [torch.cuda.Stream() for _ in range(nstreams)]
+    ws_bytes = max(m.workspace_size(B) for m in mats)
+    wss = [torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") for _ in side]
+    ys = [torch.empty((B, mat.N), dtype=torch.float32, device="cuda") for _ in side]
+    x = torch.from_numpy(mat.activations(B).view(np.int16)).cuda()
+
+    def calls(first, n):
+        for i in range(first, first + n):
+            j = i % nstreams
+            mats[i % copies].matmul(x, B, ys[j], uw.OUT_F32, uw.STRAT_AUTO, wss[j], ws_bytes, side[j])
+
+    def fork_join(first, n):
+        for sd in side:
+            sd.wait_stream(stream)
+        calls(first, n)
+        for sd in side:
+            stream.wait_stream(sd)
+
+    with torch.cuda.stream(stream):
+        fork_join(0, W + K)  # every plan warmed outside capture
+        stream.synchronize()
+        gw, gt = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw, stream=stream):
+            fork_join(0, W)
+        with torch.cuda.graph(gt, stream=stream):
+            fork_join(W, K)
+        gw.replay()
+        gt.replay()
+        stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
+    with torch.cuda.stream(stream):
+        gw.replay()
+        e0.record(stream)
+        gt.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def encode_many(recipes, threads=None):
     """Blobs of many matrices, generated and encoded on a thread pool (both run in C with the GIL released)."""
     import lossless_bf16_weight_exponent_gb300 as uw
@@ -572,12 +623,13 @@ def footprint(blob, N, K):
 
 def e2e_async(mats, mat, B, steps):
     """End-to-end throughput through uw_matmul_host_async: every step copies its X from pinned host memory, runs the
-    matmul of the autotuned plan and copies Y back into pinned host memory; two streams alternate, each with its own
-    workspace and host buffers, so one step's copies overlap another's matmul.  Timed on the host clock from the
-    first call to both streams' completion."""
+    matmul of the autotuned plan and copies Y back into pinned host memory; independent calls go round-robin to
+    three streams, each with its own workspace and host buffers, so one call's copies and start overlap other calls'
+    matmuls (with two streams a call's kernel still waited on its own copies; three keep the GPU busy).  Timed on
+    the host clock from the first call to every stream's completion."""
     import torch
     copies = len(mats)
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in range(E2E_STREAMS)]
     need = max(m.host_workspace_size(B) for m in mats)
     wss = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in streams]
     xh = [torch.from_numpy(mat.activations(B).view(np.int16)).pin_memory() for _ in streams]
@@ -585,7 +637,7 @@ def e2e_async(mats, mat, B, steps):
 
     def run(n):
         for i in range(n):
-            j = i & 1
+            j = i % len(streams)
             mats[i % copies].matmul_host_async(xh[j], B, yh[j], 0, wss[j], need, streams[j])
         for s in streams:
             s.synchronize()
@@ -707,6 +759,8 @@ def run_ours(args):
     launches_per_step = launches_per_call(plan, B)
 
     # e2e through the public API with host buffers: H2D of X and D2H of Y inside the timed region, every step
+    # the same steps as independent calls on several streams (device-timed), rank 0's extra line
+    conc_ms = concurrent_device(mats, mat, B, K, W, stream) if rank == 0 else None
     e2e_steps = min(max(K, 200), 4000)
     e2e_s = max_over_ranks(e2e_async(mats, mat, B, e2e_steps), world)
     e2e_value = job_throughput(eff_bytes, e2e_steps, world, e2e_s * 1e3)
@@ -749,7 +803,15 @@ def run_ours(args):
             "effective_frac_of_peak": value / world / hbm_peak,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": 2 * B * mat.K,
                     "d2h_bytes_per_step": 4 * B * mat.N, "us_per_call": e2e_s / e2e_steps * 1e6, "steps": e2e_steps,
-                    "api": "uw_matmul_host_async on two alternating streams, pinned host X and Y"},
+                    "api": f"uw_matmul_host_async, independent calls round-robin on {E2E_STREAMS} streams, pinned host "
+                           "X and Y"},
+            "concurrent": {"streams": E2E_STREAMS, "steps": K, "us_per_matmul": conc_ms / K * 1e3,
+                           "value": eff_bytes * K / (conc_ms * 1e-3) / 1e9, "unit": "GB/s",
+                           "compressed_frac": alg / (conc_ms / K * 1e-3) / 1e9 / hbm_peak,
+                           "effective_frac": eff_bytes / (conc_ms / K * 1e-3) / 1e9 / hbm_peak,
+                           "note": "the same matmuls as independent calls round-robin on several streams in one "
+                                   "CUDA graph (fork/join), CUDA events on the launching stream; `value` above is "
+                                   "the dependent chain on one stream"},
             "gpu_launches": launches_per_step * K,
             "clocks": clk,
             "cpu_baseline": cpu,
