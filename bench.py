@@ -543,7 +543,7 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
                                   {"gate_up": pal[0].plan_for(B).as_tuple(), "down": pal[2].plan_for(B).as_tuple()},
                                   hbm, tf_peak,
                                   {"schedule": name, "matmuls": len(mats), "hard_matmuls": hard, "decode_sms": d,
-                                   "hard_steps": ("none" if not hard else "Huffman-direct (direct schedule)"
+                                   "hard_steps": ("none" if not hard else "own AUTO plan (direct schedule)"
                                                   if d == uw.SEQ_DIRECT else "side-stream transcode"),
                                    "us_per_matmul": round(us / len(mats), 2), "time_vs_all_easy": round(us / base_us, 3),
                                    "resident_ratio": round(resident / bf16_bytes, 4),
