@@ -489,7 +489,9 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
     matmuls.  All layers easy (palette form resident, AUTO: direct palette); then hard layers (the Huffman stream
     alone) every k-th layer, run by uw_sequence_run under the schedule uw_sequence_tune picks: a side-stream
     transcode into double-buffered slots (with a decode SM split) or the direct schedule (each hard step's own AUTO
-    plan, the Huffman-direct GEMV up to B = 8); then every matrix as the Huffman stream alone under AUTO.  The
+    plan, the Huffman-direct GEMV up to B = 8); then every matrix as the Huffman stream alone under AUTO.  Each
+    pattern runs twice: every step after the one before it, and with each layer's up projection marked
+    UW_STEP_CONCURRENT beside its gate projection (both read the layer's input; up writes its own buffer).  The
     gate/up shape and the down shape are autotuned once each per form and the tables shared by shape."""
     import torch
 
@@ -516,24 +518,31 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
         x_in = torch.from_numpy(recipes[0].activations(B).view(np.int16)).cuda()            # [B, 4096]
         x_mid = torch.from_numpy(recipes[2].activations(B).view(np.int16)).cuda()           # [B, 14336]
         y_mid = torch.empty((B, 14336), dtype=torch.float32, device="cuda")
+        y_up = torch.empty((B, 14336), dtype=torch.float32, device="cuda")
         y_out = torch.empty((B, 4096), dtype=torch.float32, device="cuda")
 
-        def steps_of(mats):
-            return [(m, x_mid if i % 3 == 2 else x_in, y_out if i % 3 == 2 else y_mid, uw.OUT_F32)
-                    for i, m in enumerate(mats)]
+        def steps_of(mats, grouped):
+            return [(m, x_mid if i % 3 == 2 else x_in, (y_mid, y_up, y_out)[i % 3], uw.OUT_F32,
+                     uw.STEP_CONCURRENT if grouped and i % 3 == 1 else 0) for i, m in enumerate(mats)]
         flops = sum(2.0 * B * m.info["N"] * m.info["K"] for m in pal)
         eff = sum(2 * m.info["N"] * m.info["K"] + 2 * B * m.info["K"] + 4 * B * m.info["N"] for m in pal)
-        patterns = [("all easy", 0)] + [(f"hard every {k}", k) for k in hard_every]
+        patterns = [(name + suffix, k, grouped) for name, k in [("all easy", 0)] + [(f"hard every {k}", k)
+                                                                                  for k in hard_every]
+                    for suffix, grouped in (("", False), (", gate+up concurrent", True))]
         base_us = None
-        for name, k in patterns:
+        for name, k, grouped in patterns:
             mats = [huf[i] if k and (i // 3) % k == k - 1 else pal[i] for i in range(len(pal))]
-            steps = steps_of(mats)
+            steps = steps_of(mats, grouped)
             need = uw.sequence_workspace_size(steps, B)
             wsb = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
             wsp = (wsb.data_ptr() + 255) // 256 * 256
             hard = sum(1 for m in mats if not m.info["has_palette_form"])
-            d = uw.sequence_tune(steps, B, wsp, need, stream, side) if hard else 0  # the decode-vs-matmul SM split
-            us = time_graph(lambda i, s: uw.sequence_run(steps, B, wsp, need, s, side, d), 1, 5, stream)
+            # the schedule: the decode-vs-matmul SM split, and whether the gate/up groups overlap
+            d = uw.sequence_tune(steps, B, wsp, need, stream, side) if hard or grouped else 0
+            overlap = d >= uw.SEQ_GROUPS + uw.SEQ_DIRECT
+            d = d - uw.SEQ_GROUPS if overlap else d
+            us = time_graph(lambda i, s: uw.sequence_run(steps, B, wsp, need, s, side,
+                                                         d + (uw.SEQ_GROUPS if overlap else 0)), 1, 5, stream)
             # the transcode slots are resident while the sequence runs; the direct schedule uses none
             resident = sum(m.info["device_bytes"] for m in mats) + (need if hard and d != uw.SEQ_DIRECT else 0)
             base_us = base_us or us
@@ -543,6 +552,7 @@ def measure_stack(layers, batches, stream, hbm, tf_peak, hard_every=(8, 4, 2, 1)
                                   {"gate_up": pal[0].plan_for(B).as_tuple(), "down": pal[2].plan_for(B).as_tuple()},
                                   hbm, tf_peak,
                                   {"schedule": name, "matmuls": len(mats), "hard_matmuls": hard, "decode_sms": d,
+                                   "groups_overlapped": overlap,
                                    "hard_steps": ("none" if not hard else "own AUTO plan (direct schedule)"
                                                   if d == uw.SEQ_DIRECT else "side-stream transcode"),
                                    "us_per_matmul": round(us / len(mats), 2), "time_vs_all_easy": round(us / base_us, 3),

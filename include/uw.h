@@ -329,14 +329,21 @@ uw_status uw_tune_save(const uw_matrix *m, char *buf, size_t cap, size_t *len);
 uw_status uw_tune_load(uw_matrix *m, const char *text);
 
 /* One matmul of a sequence: Y[B,N] = X[B,K] . W^T for the loaded matrix m; x and y are device pointers as in
- * uw_matmul, out_dtype a uw_out_dtype; reserved must be 0. */
+ * uw_matmul, out_dtype a uw_out_dtype; flags 0 or UW_STEP_CONCURRENT. */
 typedef struct {
     const uw_matrix *m;
     const uint16_t *x;
     void *y;
     int32_t out_dtype;
-    int32_t reserved;
+    int32_t flags;
 } uw_step;
+
+/* The step may run at the same time as the steps before it back to the last step without the flag: it reads
+ * nothing those steps write and writes nothing they read or write (an MLP's up projection beside its gate
+ * projection: both read the layer's input).  Such a run forms a group.  The flag permits overlap; a schedule
+ * with UW_SEQ_GROUPS runs each group's matmuls on streams of their own (the first four members on four streams,
+ * any further member after the member four places before it), any other schedule runs them in order. */
+#define UW_STEP_CONCURRENT 1
 
 /*
  * uw_sequence_run - run n matmuls in order at batch B (the post's section on scheduling hard and easy layers).
@@ -350,25 +357,32 @@ typedef struct {
  *   (uw_sequence_workspace_size bytes, 256-byte aligned) belongs to the sequence until `stream` has passed it.
  *   The first call in a thread on a device creates the events the calls use; make it before any stream capture.
  *   The steps' x and y must not overlap a later step's inputs unless the caller wants that chaining: steps run in
- *   order on `stream`.
+ *   order on `stream`, except that under a UW_SEQ_GROUPS schedule a group of steps joined by UW_STEP_CONCURRENT
+ *   runs on `stream` and on streams the library keeps per thread and device (forked from and joined back to
+ *   `stream` with events, so a graph captured from `stream` holds them).  Each member of a group has its own part
+ *   of the workspace (the size covers both forms).  With the transcode schedule a hard step always waits for the
+ *   steps before it (the flag is not applied to it).
  *   Errors: UW_ERR_INVALID_ARG, UW_ERR_WORKSPACE, UW_ERR_CUDA, or a step's uw_matmul error.
  */
 /*   decode_sms: the post's decode-vs-matmul SM split.  0: every launch sizes its grid for all SMs.  d > 0: the
  *   main stream's persistent matmul grids are sized for the device's SMs minus d, and each transcode is a
  *   persistent grid of d SMs' worth of CTAs, so the two run side by side.  UW_SEQ_DIRECT (-1): no side-stream
  *   transcode; every step runs its own AUTO plan on `stream` (a hard step at B <= 8: the Huffman-direct GEMV;
- *   `side_stream` is not used).  Must lie in [-1, SMs).
+ *   `side_stream` is not used).  Any of these plus UW_SEQ_GROUPS: the same schedule with the groups of
+ *   UW_STEP_CONCURRENT steps overlapped.  Must lie in [-1, SMs) or in UW_SEQ_GROUPS + [-1, SMs).
  */
 #define UW_SEQ_DIRECT (-1)
+#define UW_SEQ_GROUPS 65536
 uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int64_t B, size_t *bytes);
 uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
                           uw_stream side_stream, int decode_sms);
 
 /*
  * uw_sequence_tune - time uw_sequence_run over these steps (same arguments) for the direct schedule and a range of
- *   decode SM splits (UW_SEQ_DIRECT, 0, 8, 16, ..., 96; CUDA events on `stream`, median of three runs after two)
- *   and return the fastest in *decode_sms (the post's tuning of the decoder's share of the SMs).  Synchronous;
- *   runs the sequence 5 times per candidate, writing the steps' outputs.
+ *   decode SM splits (UW_SEQ_DIRECT, 0, 8, 16, ..., 96; CUDA events on `stream`, median of three runs after two),
+ *   each also with UW_SEQ_GROUPS when a step carries UW_STEP_CONCURRENT, and return the fastest in *decode_sms
+ *   (the post's tuning of the decoder's share of the SMs).  Synchronous; runs the sequence 5 times per
+ *   candidate, writing the steps' outputs.
  */
 uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, void *workspace, size_t ws_bytes, uw_stream stream,
                            uw_stream side_stream, int *decode_sms);

@@ -30,6 +30,8 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_TC = 0, 1, 2
 RESIDENT_HUFFMAN, RESIDENT_BOTH, RESIDENT_PALETTE = 0, 1, 2
 RESIDENT = {"huffman": RESIDENT_HUFFMAN, "both": RESIDENT_BOTH, "palette": RESIDENT_PALETTE}
 SEQ_DIRECT = -1  # uw_sequence_run schedule: no side-stream transcode, every step its own AUTO plan
+STEP_CONCURRENT = 1  # uw_step flag: the step may overlap the step before it
+SEQ_GROUPS = 65536  # added to a uw_sequence_run schedule: overlap the groups of STEP_CONCURRENT steps
 
 
 class UwError(RuntimeError):
@@ -56,7 +58,7 @@ class Plan(ctypes.Structure):
 
 class Step(ctypes.Structure):
     _fields_ = [("m", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("out_dtype", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class Info(ctypes.Structure):
@@ -279,12 +281,13 @@ def _steps(steps):
     for i, st in enumerate(steps):
         m, x, y = st[0], st[1], st[2]
         od = st[3] if len(st) > 3 else OUT_F32
-        arr[i] = Step(m.handle.value if isinstance(m, Matrix) else m, _ptr(x), _ptr(y), od, 0)
+        fl = st[4] if len(st) > 4 else 0
+        arr[i] = Step(m.handle.value if isinstance(m, Matrix) else m, _ptr(x), _ptr(y), od, fl)
     return arr
 
 
 def sequence_workspace_size(steps, B: int) -> int:
-    """Workspace bytes of uw_sequence_run; steps: (Matrix, x, y[, out_dtype]) tuples."""
+    """Workspace bytes of uw_sequence_run; steps: (Matrix, x, y[, out_dtype[, flags]]) tuples."""
     n = ctypes.c_size_t(0)
     _check(lib().uw_sequence_workspace_size(_steps(steps), len(steps), B, ctypes.byref(n)), "uw_sequence_workspace_size")
     return n.value

@@ -18,6 +18,13 @@
 // batch 8 or less, the GEMV that decodes the Huffman stream inside the product).  uw_sequence_tune times these
 // schedules and returns the fastest: when a matmul already holds HBM at its peak, a transcode beside it cannot
 // hide, and decoding inside the product costs less than transcoding first.
+//
+// Steps the caller marks UW_STEP_CONCURRENT may overlap the step before them (an MLP's gate and up projections
+// read the same input).  On one stream each matmul waits for the whole preceding grid (its output may be the next
+// one's input), its prologue overlapped with that grid's end by programmatic dependent launch; a UW_SEQ_GROUPS
+// schedule instead runs a group of independent steps on the main stream and up to three streams of the library's
+// own, forked and joined with events, so that the members overlap each other, at the cost of full dependencies
+// at the fork and the join.  Which wins depends on the shapes and B, so the tuner times both.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,17 +44,24 @@ bool is_hard(const uw_matrix *m) { return m->codes == nullptr && m->has_stream; 
 
 uint64_t slot_bytes_of(const uw_matrix *m) { return round_up((uint64_t)m->h.N * (uint64_t)m->h.K / 2 + 64, 256); }
 
+constexpr int kLanes = 4;  // streams a group of concurrent steps runs on: the caller's and three of the library's
+
 struct Layout {
     uint64_t slot;  // bytes of one preprocess slot (the largest hard matrix's codes)
-    uint64_t mm;    // bytes of the matmul workspace (the largest any step needs)
+    uint64_t mm;    // bytes of one lane's matmul workspace (the largest any step needs)
     int hard;       // hard steps
+    int lanes;      // lanes the largest group of concurrent steps needs (each has its own matmul workspace)
 };
 
 uw_status layout_of(const uw_step *steps, int n, int64_t B, Layout *L)
 {
     L->slot = L->mm = 0;
     L->hard = 0;
-    for (int i = 0; i < n; i++) {
+    L->lanes = 1;
+    for (int i = 0, g = 0; i < n; i++) {
+        g = (i > 0 && (steps[i].flags & UW_STEP_CONCURRENT)) ? g + 1 : 1;
+        L->lanes = std::max(L->lanes, std::min(g, kLanes));
+        if (steps[i].flags & ~UW_STEP_CONCURRENT) return fail(UW_ERR_INVALID_ARG, "uw_sequence: step %d has unknown flags", i);
         const uw_matrix *m = steps[i].m;
         if (!m) return fail(UW_ERR_INVALID_ARG, "uw_sequence: step %d has no matrix", i);
         if (is_hard(m)) {
@@ -69,11 +83,11 @@ uw_status layout_of(const uw_step *steps, int n, int64_t B, Layout *L)
     return UW_OK;
 }
 
-// The six events a sequence uses, one set per thread and device, created by the thread's first call on that
-// device and kept (a call captured into a CUDA graph then creates nothing).  Reusing them across calls is safe: a
+// The events a sequence uses, one set per thread and device, created by the thread's first call on that device
+// and kept (a call captured into a CUDA graph then creates nothing).  Reusing them across calls is safe: a
 // stream wait binds to the event's latest record when the wait is enqueued, and every wait of a call follows its
 // own records.
-using EventSet = std::array<cudaEvent_t, 6>;
+using EventSet = std::array<cudaEvent_t, 6 + kLanes>;  // start, ready[2], freed[2], done, fork, join[kLanes - 1]
 uw_status thread_events(EventSet **out)
 {
     thread_local std::vector<std::pair<int, EventSet>> sets;
@@ -94,6 +108,28 @@ uw_status thread_events(EventSet **out)
     return UW_OK;
 }
 
+// The library's streams for groups of concurrent steps, kLanes - 1 per thread and device, created with the events.
+using LaneStreams = std::array<cudaStream_t, kLanes - 1>;
+uw_status thread_lanes(LaneStreams **out)
+{
+    thread_local std::vector<std::pair<int, LaneStreams>> sets;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(UW_ERR_CUDA, "uw_sequence_run: cudaGetDevice: %s", cudaGetErrorString(e));
+    for (auto &p : sets)
+        if (p.first == dev) { *out = &p.second; return UW_OK; }
+    LaneStreams ls{};
+    for (auto &st : ls)
+        if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) {
+            for (auto &d : ls)
+                if (d) cudaStreamDestroy(d);
+            return fail(UW_ERR_CUDA, "uw_sequence_run: stream creation: %s", cudaGetErrorString(e));
+        }
+    sets.emplace_back(dev, ls);
+    *out = &sets.back().second;
+    return UW_OK;
+}
+
 }  // namespace
 
 extern "C" uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int64_t B, size_t *bytes)
@@ -103,7 +139,7 @@ extern "C" uw_status uw_sequence_workspace_size(const uw_step *steps, int n, int
     Layout L;
     uw_status s = layout_of(steps, n, B, &L);
     if (s != UW_OK) return s;
-    *bytes = (L.hard ? 2 * L.slot : 0) + L.mm;
+    *bytes = (L.hard ? 2 * L.slot : 0) + L.mm * (uint64_t)L.lanes;
     return UW_OK;
 }
 
@@ -112,13 +148,15 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
 {
     clear_error();
     if (n < 0 || (n && !steps) || B < 0) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: bad arguments");
+    const bool groups = decode_sms >= UW_SEQ_GROUPS + UW_SEQ_DIRECT;
+    if (groups) decode_sms -= UW_SEQ_GROUPS;
     if (decode_sms < UW_SEQ_DIRECT || decode_sms >= device_sms())
         return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: decode_sms %d outside [-1, %d)", decode_sms, device_sms());
     if (n == 0 || B == 0) return UW_OK;
     Layout L;
     uw_status s = layout_of(steps, n, B, &L);
     if (s != UW_OK) return s;
-    const uint64_t need = (L.hard ? 2 * L.slot : 0) + L.mm;
+    const uint64_t need = (L.hard ? 2 * L.slot : 0) + L.mm * (uint64_t)L.lanes;
     if (ws_bytes < need || (need && !ws)) return fail(UW_ERR_WORKSPACE, "uw_sequence_run: workspace %zu bytes, need %llu", ws_bytes, (unsigned long long)need);
     if (ws && ((uintptr_t)ws & 255)) return fail(UW_ERR_INVALID_ARG, "uw_sequence_run: workspace not 256-byte aligned");
     if (L.hard && decode_sms != UW_SEQ_DIRECT && stream == side_stream)
@@ -129,29 +167,70 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
     uint8_t *slot[2] = {(uint8_t *)ws, (uint8_t *)ws + L.slot};
     uint8_t *mm = (uint8_t *)ws + (L.hard ? 2 * L.slot : 0);
     cudaStream_t main = (cudaStream_t)stream, side = (cudaStream_t)side_stream;
+    const bool transcode = L.hard && decode_sms != UW_SEQ_DIRECT;
 
-    if (!L.hard || decode_sms == UW_SEQ_DIRECT) {
-        for (int i = 0; i < n; i++) {
-            s = uw_matmul(steps[i].m, steps[i].x, B, steps[i].y, (uw_out_dtype)steps[i].out_dtype, UW_STRAT_AUTO, mm, L.mm,
-                          stream);
-            if (s != UW_OK) return s;
+    EventSet *ev = nullptr;
+    s = thread_events(&ev);
+    if (s != UW_OK) return s;
+    LaneStreams *lanes = nullptr;
+    if (groups && L.lanes > 1 && (s = thread_lanes(&lanes)) != UW_OK) return s;
+    cudaEvent_t start = (*ev)[0], ready[2] = {(*ev)[1], (*ev)[2]}, freed[2] = {(*ev)[3], (*ev)[4]}, done = (*ev)[5];
+    cudaEvent_t fork = (*ev)[6];
+    // the split: the matmuls' grids for the SMs left, the transcode's for d SMs
+    SmBudget budget(decode_sms > 0 ? device_sms() - decode_sms : 0);
+    const int decode_ctas = decode_sms > 0 ? decode_sms * kDecodeCtasPerSm : 0;
+    cudaError_t e = cudaSuccess;
+
+    // steps [i0, i1), which the caller marked concurrent after i0: the main stream and the lanes, each member
+    // with its own matmul workspace; a single step runs on the main stream
+    auto run_group = [&](int i0, int i1) -> uw_status {
+        const int n_g = i1 - i0;
+        const int used = std::min(n_g, kLanes);
+        if (used > 1) {
+            if ((e = cudaEventRecord(fork, main)) != cudaSuccess) return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
+            for (int l = 1; l < used; l++)
+                if ((e = cudaStreamWaitEvent((*lanes)[l - 1], fork, 0)) != cudaSuccess)
+                    return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
+        }
+        for (int j = 0; j < n_g; j++) {
+            const int l = j % kLanes;
+            const uw_step &st = steps[i0 + j];
+            cudaStream_t sl = l ? (*lanes)[l - 1] : main;
+            uw_status r = uw_matmul(st.m, st.x, B, st.y, (uw_out_dtype)st.out_dtype, UW_STRAT_AUTO, mm + (uint64_t)l * L.mm,
+                                    L.mm, (uw_stream)sl);
+            if (r != UW_OK) return r;
+        }
+        for (int l = 1; l < used; l++) {
+            cudaEvent_t join = (*ev)[6 + l];
+            if ((e = cudaEventRecord(join, (*lanes)[l - 1])) != cudaSuccess || (e = cudaStreamWaitEvent(main, join, 0)) != cudaSuccess)
+                return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
         }
         return UW_OK;
+    };
+    // where the group starting at step i ends: the run of steps marked concurrent after it (without UW_SEQ_GROUPS,
+    // and for a hard step of the transcode schedule, the step alone)
+    auto group_end = [&](int i) {
+        if (!groups || (transcode && is_hard(steps[i].m))) return i + 1;
+        int j = i + 1;
+        while (j < n && (steps[j].flags & UW_STEP_CONCURRENT) && !(transcode && is_hard(steps[j].m))) j++;
+        return j;
+    };
+
+    if (!transcode) {
+        for (int i = 0; i < n && s == UW_OK;) {
+            const int j = group_end(i);
+            s = run_group(i, j);
+            i = j;
+        }
+        return s;
     }
 
     // events: the side stream starts after the work already on the main stream; ready[k] - slot k holds the codes of
     // the hard step that uses it next; freed[k] - the matmul that read slot k is done; done - the side stream's end
-    EventSet *ev = nullptr;
-    s = thread_events(&ev);
-    if (s != UW_OK) return s;
-    cudaEvent_t start = (*ev)[0], ready[2] = {(*ev)[1], (*ev)[2]}, freed[2] = {(*ev)[3], (*ev)[4]}, done = (*ev)[5];
     std::vector<int> hard;
     for (int i = 0; i < n; i++)
         if (is_hard(steps[i].m)) hard.push_back(i);
-    // the split: the matmuls' grids for the SMs left, the transcode's for d SMs
-    SmBudget budget(decode_sms ? device_sms() - decode_sms : 0);
-    const int decode_ctas = decode_sms * kDecodeCtasPerSm;
-    cudaError_t e = cudaEventRecord(start, main);
+    e = cudaEventRecord(start, main);
     if (!e) e = cudaStreamWaitEvent(side, start, 0);
     // the transcode of hard step j into slot j % 2, on the side stream, once the matmul of hard step j - 2 is done
     auto enqueue_transcode = [&](int j) -> cudaError_t {
@@ -164,7 +243,7 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
     };
     for (int j = 0; j < std::min<int>(2, (int)hard.size()) && !e; j++) e = enqueue_transcode(j);
     int hj = 0;
-    for (int i = 0; i < n && !e && s == UW_OK; i++) {
+    for (int i = 0; i < n && !e && s == UW_OK;) {
         const uw_step &st = steps[i];
         if (hj < (int)hard.size() && hard[hj] == i) {
             const int k = hj & 1;
@@ -173,8 +252,11 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
             if (!e && s == UW_OK) e = cudaEventRecord(freed[k], main);
             if (!e && s == UW_OK && hj + 2 < (int)hard.size()) e = enqueue_transcode(hj + 2);
             hj++;
+            i++;
         } else {
-            s = uw_matmul(st.m, st.x, B, st.y, (uw_out_dtype)st.out_dtype, UW_STRAT_AUTO, mm, L.mm, stream);
+            const int j = group_end(i);
+            s = run_group(i, j);
+            i = j;
         }
     }
     // join: the main stream ends after the side stream's last transcode
@@ -198,32 +280,72 @@ extern "C" uw_status uw_sequence_tune(const uw_step *steps, int n, int64_t B, vo
         return fail(UW_ERR_CUDA, "uw_sequence_tune: event creation failed");
     }
     const int sms = device_sms();
-    float best = 3.0e38f;
-    uw_status result = UW_OK;
-    for (int d : {UW_SEQ_DIRECT, 0, 8, 16, 24, 32, 40, 48, 64, 80, 96}) {
-        if (d >= sms) continue;
-        float t[3];
-        bool ok = true;
-        for (int r = 0; r < 5 && ok; r++) {
-            if (r >= 2) cudaEventRecord(e0, main);
-            uw_status s = uw_sequence_run(steps, n, B, ws, ws_bytes, stream, side_stream, d);
+    bool flagged = false;
+    for (int i = 1; i < n; i++) flagged |= (steps[i].flags & UW_STEP_CONCURRENT) != 0;
+    std::vector<int> cand;
+    for (int g : {0, UW_SEQ_GROUPS})
+        if (g == 0 || flagged)
+            for (int d : {UW_SEQ_DIRECT, 0, 8, 16, 24, 32, 40, 48, 64, 80, 96})
+                if (d < sms) cand.push_back(g + d);
+    // one candidate: an eager run (checks it and creates the thread's events and streams), then the sequence
+    // captured into a graph, two replays, and three bursts of three replays timed; where `stream` cannot be
+    // captured (the legacy default stream), five eager runs, the last three timed
+    auto timed = [&](int d, float *ms) -> uw_status {
+        uw_status s = uw_sequence_run(steps, n, B, ws, ws_bytes, stream, side_stream, d);
+        if (s != UW_OK) return s;
+        cudaGraph_t g = nullptr;
+        cudaGraphExec_t ge = nullptr;
+        if (cudaStreamBeginCapture(main, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+            s = uw_sequence_run(steps, n, B, ws, ws_bytes, stream, side_stream, d);
+            cudaError_t e = cudaStreamEndCapture(main, &g);
             if (s != UW_OK) {
-                if (d == 0) result = s;
-                ok = false;
-                break;
+                if (g) cudaGraphDestroy(g);
+                return s;
             }
+            if (e != cudaSuccess || cudaGraphInstantiate(&ge, g, 0) != cudaSuccess) ge = nullptr;
+        }
+        cudaGetLastError();  // a refused capture leaves its error behind; the eager timing below stands in
+        float t[3];
+        for (int r = 0; r < 5; r++) {
+            if (r >= 2) cudaEventRecord(e0, main);
+            for (int k = 0; k < (ge && r >= 2 ? 3 : 1); k++) {
+                if (ge) {
+                    if (cudaGraphLaunch(ge, main) != cudaSuccess) s = fail(UW_ERR_CUDA, "uw_sequence_tune: graph launch failed");
+                } else {
+                    s = uw_sequence_run(steps, n, B, ws, ws_bytes, stream, side_stream, d);
+                }
+                if (s != UW_OK) break;
+            }
+            if (s != UW_OK) break;
             if (r >= 2) {
                 cudaEventRecord(e1, main);
-                if (cudaEventSynchronize(e1) != cudaSuccess) { ok = false; break; }
+                if (cudaEventSynchronize(e1) != cudaSuccess) {
+                    s = fail(UW_ERR_CUDA, "uw_sequence_tune: %s", cudaGetErrorString(cudaGetLastError()));
+                    break;
+                }
                 cudaEventElapsedTime(&t[r - 2], e0, e1);
             }
         }
-        if (!ok) {
-            if (result != UW_OK) break;
-            continue;
-        }
+        if (ge) cudaGraphExecDestroy(ge);
+        if (g) cudaGraphDestroy(g);
+        if (s != UW_OK) return s;
         std::sort(t, t + 3);
-        if (t[1] < best * 0.99f) { best = t[1]; *decode_sms = d; }
+        *ms = t[1];
+        return UW_OK;
+    };
+    float best = 3.0e38f;
+    uw_status result = UW_OK;
+    for (int d : cand) {
+        float ms = 0.0f;
+        uw_status s = timed(d, &ms);
+        if (s != UW_OK) {
+            if (d == 0 || s == UW_ERR_CUDA) {  // the plain schedule must run; a CUDA error ends the search
+                result = s;
+                break;
+            }
+            continue;  // a split this sequence cannot take (a budget too small for a kernel)
+        }
+        if (ms < best * 0.99f) { best = ms; *decode_sms = d; }
     }
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
