@@ -192,20 +192,21 @@ extern "C" uw_status uw_sequence_run(const uw_step *steps, int n, int64_t B, voi
                 if ((e = cudaStreamWaitEvent((*lanes)[l - 1], fork, 0)) != cudaSuccess)
                     return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
         }
-        for (int j = 0; j < n_g; j++) {
+        uw_status r = UW_OK;
+        for (int j = 0; j < n_g && r == UW_OK; j++) {
             const int l = j % kLanes;
             const uw_step &st = steps[i0 + j];
             cudaStream_t sl = l ? (*lanes)[l - 1] : main;
-            uw_status r = uw_matmul(st.m, st.x, B, st.y, (uw_out_dtype)st.out_dtype, UW_STRAT_AUTO, mm + (uint64_t)l * L.mm,
-                                    L.mm, (uw_stream)sl);
-            if (r != UW_OK) return r;
+            r = uw_matmul(st.m, st.x, B, st.y, (uw_out_dtype)st.out_dtype, UW_STRAT_AUTO, mm + (uint64_t)l * L.mm, L.mm,
+                          (uw_stream)sl);
         }
+        // join every forked lane, also after a failed step, so that a capture from the main stream stays joined
         for (int l = 1; l < used; l++) {
             cudaEvent_t join = (*ev)[6 + l];
             if ((e = cudaEventRecord(join, (*lanes)[l - 1])) != cudaSuccess || (e = cudaStreamWaitEvent(main, join, 0)) != cudaSuccess)
-                return fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
+                return r != UW_OK ? r : fail(UW_ERR_CUDA, "uw_sequence_run: %s", cudaGetErrorString(e));
         }
-        return UW_OK;
+        return r;
     };
     // where the group starting at step i ends: the run of steps marked concurrent after it (without UW_SEQ_GROUPS,
     // and for a hard step of the transcode schedule, the step alone)
