@@ -54,6 +54,22 @@ def test_binding_constants_match_the_header():
                                               if k.startswith("UW_STRAT_") and k != "UW_STRAT_AUTO"]
 
 
+def test_binding_defines_and_step_layout_match_the_header():
+    # the sequence runner's #define constants, and the uw_step struct the binding fills for it
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(uw.LIB_PATH), "..", "include", "uw.h")).read()
+    d = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(UW_[A-Z0-9_]+)\s+\(?(-?\d+)\)?", src)}
+    assert d == {"UW_STEP_CONCURRENT": uw.STEP_CONCURRENT, "UW_SEQ_DIRECT": uw.SEQ_DIRECT,
+                 "UW_SEQ_GROUPS": uw.SEQ_GROUPS}
+    body = re.search(r"typedef struct \{([^}]*)\} uw_step;", src).group(1)
+    fields = [re.sub(r"[;*]", " ", ln).split()[-1] for ln in body.strip().splitlines() if ln.strip()]
+    assert fields == [f[0] for f in uw.Step._fields_] == ["m", "x", "y", "out_dtype", "flags"]
+    assert ctypes.sizeof(uw.Step) == 32 and uw.Step.out_dtype.offset == 24 and uw.Step.flags.offset == 28
+    # a direct schedule with groups stays distinguishable from every plain schedule
+    assert uw.SEQ_GROUPS + uw.SEQ_DIRECT > 1 << 15
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(uw, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(uw, "_lib", None)
